@@ -1,0 +1,64 @@
+"""The seeded input generator against SplitMix64's sequential definition."""
+import numpy as np
+
+import seeded_inputs as si
+
+MASK = (1 << 64) - 1
+
+
+def _mix_py(z):
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK
+    return z ^ (z >> 31)
+
+
+def _sequential(state, count):
+    out = []
+    for _ in range(count):
+        state = (state + 0x9E3779B97F4A7C15) & MASK
+        out.append(_mix_py(state))
+    return out
+
+
+def test_counter_form_equals_sequential_generator():
+    for state in (0, 1, 1234567, (1 << 64) - 1):
+        got = [int(v) for v in si.splitmix64_sequence(state, 9)]
+        assert got == _sequential(state, 9)
+
+
+def test_streams_use_their_own_base_and_offsets():
+    base = int(si.stream_base(5, 3))
+    assert base == _mix_py((5 * (1 << 20) + 3) & MASK)
+    whole = si.stream_bits(5, 3, 40)
+    assert [int(v) for v in whole] == _sequential(base, 40)
+    assert np.array_equal(si.stream_bits(5, 3, 10, offset=30), whole[30:])
+
+
+def test_value_maps():
+    u = si.uniform_pm1(1, 0, (1000,))
+    assert u.dtype == np.float32 and u.min() >= -1.0 and u.max() < 1.0
+    # every value is a multiple of 2**-23 (24-bit grid on [-1, 1))
+    assert np.all(np.round(u.astype(np.float64) * 2 ** 23) == u.astype(np.float64) * 2 ** 23)
+    z = si.integers(1, 1, (5000,))
+    assert set(np.unique(z).tolist()) == set(range(-4, 5))
+    n = si.normal(1, 2, (200000,), sd=0.5)
+    assert abs(float(n.mean())) < 0.01 and abs(float(n.std()) - 0.5) < 0.01
+
+
+def test_chunked_generation_matches_unchunked(monkeypatch):
+    a = si.uniform_pm1(9, 1, (3, 1000))
+    monkeypatch.setattr(si, "_CHUNK", 257)
+    b = si.uniform_pm1(9, 1, (3, 1000))
+    assert np.array_equal(a, b)
+    c = si.normal(9, 1, (3, 1000))
+    monkeypatch.setattr(si, "_CHUNK", 1 << 22)
+    assert np.array_equal(c, si.normal(9, 1, (3, 1000)))
+
+
+def test_workload_table():
+    w = si.workload("sgemm_8192")
+    assert (w.M, w.N, w.K, w.alpha, w.beta, w.seed) == (8192, 8192, 8192, 0.75, 0.25, 2)
+    w = si.workload("sgemm_3001x5003x1999")
+    assert (w.M, w.N, w.K) == (3001, 5003, 1999)
+    r, c = si.workload("sgemm_16384").samples()
+    assert r.min() >= 0 and r.max() < 16384 and c.max() == 16383 and len(r) >= 4096
