@@ -1,0 +1,180 @@
+/*
+ * libphobos_gemm -- fp32 GEMM  C = alpha * A * B + beta * C  on one GB300
+ * (sm_103a), as a C ABI.
+ *
+ * The operation is the tiled matrix multiply that the Phobos pages use as
+ * their running example: the `matmul` kernel of the "@cluster" attribute page
+ * (phobos-lang.dev, "What the cluster compiler accepts": an accumulator tile
+ * summed over a K loop, stored once as alpha * acc + beta * c_old) and the
+ * "Matrix Multiplication" section of "Show HN: Phobos - A tiny scale-free
+ * kernel language with tile-DAG support" (C = alpha A B + beta C with A of
+ * M x K, B of K x N, C of M x N).
+ *
+ * Conventions shared by every entry point:
+ *  - Layout: all matrices are row-major.  A[i][k] = A[i*lda + k],
+ *    B[k][j] = B[k*ldb + j], C[i][j] = C[i*ldc + j].  Any size and leading
+ *    dimension is accepted (the pages' multiple-of-four restriction is lifted)
+ *    provided lda >= max(1,K), ldb >= max(1,N), ldc >= max(1,N).
+ *  - Degenerate sizes: M == 0 or N == 0 is a no-op.  K == 0 or alpha == 0
+ *    gives C = beta * C (an empty sum is zero).  beta == 0 means C is not read
+ *    (so NaN or garbage in C is overwritten), following the init leaf of the
+ *    cluster split, which "zeroes the output super-tile, or scales it by beta".
+ *  - Ownership: A, B and C are caller-owned device pointers; the library never
+ *    frees or retains them.  A and B are read only.  C must not overlap A or B
+ *    (not checked; the result is undefined).  The library owns its workspace
+ *    (per device and stream, grown on demand, released by phobos_release).
+ *  - Execution: asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).  The call returns after enqueueing.
+ *    The current device must be compute capability 10.3 (sm_103); there is no
+ *    CPU fallback.
+ *  - Errors: a phobos_status_t; nothing is enqueued when the status is not
+ *    PHOBOS_OK, except that PHOBOS_ERR_CUDA may follow a partial enqueue.
+ *    Device-side bounded waits that expire set a device status word; it is
+ *    read (and cleared) by phobos_check_device, and by every call when the
+ *    environment variable PHOBOS_DEBUG_SYNC=1 is set.
+ *  - Thread safety: calls may come from several host threads.  Calls that
+ *    share one stream are ordered by it; calls on different streams use
+ *    different workspaces.
+ */
+#ifndef PHOBOS_GEMM_H
+#define PHOBOS_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PHOBOS_OK = 0,
+  PHOBOS_ERR_INVALID_VALUE = 1, /* negative size, small leading dimension, NULL pointer, bad plan */
+  PHOBOS_ERR_UNSUPPORTED = 2,   /* device is not sm_103, or the plan cannot run this shape */
+  PHOBOS_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+  PHOBOS_ERR_OUT_OF_MEMORY = 4, /* the workspace could not be allocated */
+  PHOBOS_ERR_TIMEOUT = 5        /* a device-side bounded wait expired (see phobos_check_device) */
+} phobos_status_t;
+
+/* How the products are formed.  DEFAULT picks FFMA for small problems and
+ * split TF32 (3xTF32) on the tensor cores otherwise. */
+typedef enum {
+  PHOBOS_MATH_DEFAULT = 0,
+  PHOBOS_MATH_3XTF32 = 1, /* a = a_big + a_small, three tf32 products, fp32-level accuracy */
+  PHOBOS_MATH_TF32 = 2,   /* one tf32 product per term (10-bit mantissa operands) */
+  PHOBOS_MATH_FFMA = 3    /* fp32 fused multiply-add on the CUDA cores */
+} phobos_math_t;
+
+typedef enum {
+  PHOBOS_PATH_FFMA = 1,
+  PHOBOS_PATH_TF32 = 2,
+  PHOBOS_PATH_3XTF32 = 3
+} phobos_path_t;
+
+/*
+ * A plan: which kernel runs and how the problem is tiled.
+ *  path            phobos_path_t.
+ *  tile_m, tile_n  output tile of one CTA (tile_m = 256 for a 2-CTA pair).
+ *  tile_k          K depth of one shared-memory stage.
+ *  cluster_m/_n    CTAs per thread-block cluster along M and N (1 x 1 or 2 x 1).
+ *  stages          depth of the shared-memory ring.
+ *  multicast       1 if operand panels are TMA-multicast inside a cluster.
+ *  super_m/_n      super-tile: the output tiles are walked super-tile by
+ *                  super-tile (an L2-locality group on one GPU).
+ *  super_k         K chunk of the cluster split: super_k < K runs an init
+ *                  leaf C = beta*C then one step leaf C += alpha*A_c*B_c per
+ *                  chunk (results equal up to rounding order).
+ *  workspace_bytes device workspace the call needs.
+ */
+typedef struct {
+  int32_t path;
+  int32_t tile_m, tile_n, tile_k;
+  int32_t cluster_m, cluster_n;
+  int32_t stages;
+  int32_t multicast;
+  int64_t super_m, super_n, super_k;
+  size_t workspace_bytes;
+} phobos_gemm_plan_t;
+
+/*
+ * Choose a plan for an M x N x K problem with the given leading dimensions and
+ * math mode (host logic only; no device call).  Tile choice follows the
+ * pages' split into CTA tiles (@autotune) and super-tiles (@cluster): "@cluster"
+ * attribute page, "A minimal kernel" and "What runs today" (a dimension takes
+ * its first value without tuning); "Show HN: Phobos", "Clustering".
+ * Errors: PHOBOS_ERR_INVALID_VALUE for bad sizes/leading dimensions, an
+ * unknown math mode or out == NULL.
+ */
+phobos_status_t phobos_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda,
+                                 int64_t ldb, int64_t ldc, phobos_math_t math,
+                                 phobos_gemm_plan_t *out);
+
+/*
+ * C = alpha * A * B + beta * C with the default math mode and an automatic
+ * plan.  See the conventions above for layout, ownership and errors.
+ * Definition: "@cluster" attribute page, the `matmul` listing; "Show HN:
+ * Phobos", "Matrix Multiplication".
+ */
+phobos_status_t phobos_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
+                             const float *A, int64_t lda, const float *B,
+                             int64_t ldb, float beta, float *C, int64_t ldc,
+                             void *stream);
+
+/*
+ * As phobos_sgemm with an explicit math mode and, optionally, a plan (NULL =
+ * automatic).  A caller-supplied plan is validated against the shape and the
+ * mode; PHOBOS_ERR_INVALID_VALUE if it does not fit.  A plan with
+ * super_k < K runs the cluster split of the "@cluster" page ("the init leaf
+ * zeroes the output super-tile, or scales it by beta, and the step leaf adds
+ * one chunk of K per launch"; "Show HN: Phobos", "Clustering": the beta term
+ * is hoisted into the init leaf and each chunk applies an implicit beta of 1).
+ */
+phobos_status_t phobos_sgemm_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                                const float *A, int64_t lda, const float *B,
+                                int64_t ldb, float beta, float *C, int64_t ldc,
+                                void *stream, phobos_math_t math,
+                                const phobos_gemm_plan_t *plan);
+
+/*
+ * Host-buffer form: A, B and C are HOST pointers (pinned memory gives the
+ * fastest copies).  The call copies A, B (and C when beta != 0) to device
+ * buffers owned by the library, runs phobos_sgemm_ex on `stream`, copies C back
+ * and synchronizes `stream` before returning.  Same layout and errors as
+ * phobos_sgemm_ex, plus PHOBOS_ERR_OUT_OF_MEMORY for the staging buffers.
+ */
+phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha,
+                                  const float *A, int64_t lda, const float *B,
+                                  int64_t ldb, float beta, float *C, int64_t ldc,
+                                  void *stream, phobos_math_t math);
+
+/*
+ * Synchronize `stream`, then read and clear the device status word of the
+ * current device.  PHOBOS_ERR_TIMEOUT if a kernel's bounded wait expired since
+ * the last check, PHOBOS_ERR_CUDA if synchronization failed, else PHOBOS_OK.
+ */
+phobos_status_t phobos_check_device(void *stream);
+
+/*
+ * Instrumentation.  With non-NULL events (cudaEvent_t passed as void*), every
+ * following call of this library on any stream records `start` on its stream
+ * just before its main GEMM kernel (after the operand pre-pass, if any) and
+ * `stop` just after the last main kernel, so that cudaEventElapsedTime gives
+ * the main kernel's device time.  NULL, NULL switches recording off.  The
+ * events stay owned by the caller.  Always PHOBOS_OK.
+ */
+phobos_status_t phobos_set_timing_events(void *start, void *stop);
+
+/* Number of CUDA kernels this library has launched since it was loaded. */
+uint64_t phobos_kernel_launches(void);
+
+/* Free every workspace and staging buffer the library holds (all devices).
+ * Must not be called while a call of this library is running on any stream. */
+phobos_status_t phobos_release(void);
+
+/* A static, NUL-terminated description of a status code. */
+const char *phobos_status_string(phobos_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PHOBOS_GEMM_H */

@@ -1,0 +1,54 @@
+// Internal launch interface between the C ABI (phobos_gemm.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace phobos {
+
+// ---------------------------------------------------------------- FFMA path
+struct FfmaArgs {
+  const float *A;
+  const float *B;
+  float *C;
+  int64_t lda, ldb, ldc;
+  int M, N, K;
+  float alpha, beta;
+  int tile;        // 128 (128x128 tile, 256 threads) or 64 (64x64 tile, 64 threads)
+  int k_begin;     // first k of this launch
+  int k_len;       // number of k of this launch
+  int vec_a, vec_b, vec_c;  // 16-byte vector access allowed for A / B / C
+};
+cudaError_t launch_ffma(const FfmaArgs &a, cudaStream_t stream);
+
+// ------------------------------------------------------ split / pack pre-pass
+// A (M x K, row-major, lda) -> big/small [Mp][Kp]; zero padding.
+cudaError_t launch_split_rows(const float *A, int64_t lda, int M, int K, int Mp, int Kp,
+                              float *big, float *small, int vec, cudaStream_t stream);
+// B (K x N, row-major, ldb) -> transposed big/small [Np][Kp] (K-major); zero padding.
+cudaError_t launch_split_cols(const float *B, int64_t ldb, int K, int N, int Np, int Kp,
+                              float *big, float *small, cudaStream_t stream);
+// C = beta * C (beta == 0: C = 0 without reading C).
+cudaError_t launch_scale(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);
+
+// ------------------------------------------------------- tensor-core path
+struct TcArgs {
+  CUtensorMap tmap_ab, tmap_as, tmap_bb, tmap_bs;  // K-major operand maps
+  float *C;
+  int64_t ldc;
+  int M, N;
+  int k_block0, k_blocks;  // BK = 32 blocks of this launch
+  int tiles_m, tiles_n, group_m;
+  float alpha, beta;
+  int vec_c;
+  int promote_blocks;  // K blocks per TMEM partial sum before it is added into registers
+  int *err;
+};
+// passes: 1 (tf32) or 3 (split tf32); bn: 128 or 256.
+cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream);
+int tc_max_stages(int passes, int bn);
+
+}  // namespace phobos

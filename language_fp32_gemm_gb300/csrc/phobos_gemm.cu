@@ -1,0 +1,532 @@
+// C ABI of libphobos_gemm: argument checks, the planner, workspace handling
+// and dispatch to the FFMA and tensor-core kernels.  See include/phobos_gemm.h
+// for the contract of every entry point.
+#include "../../include/phobos_gemm.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "internal.h"
+
+namespace phobos {
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;  // kernels index with int
+constexpr int kTcBK = 32;
+constexpr int kTcBM = 128;
+constexpr int64_t kFfmaMacLimit = int64_t{1} << 25;     // DEFAULT: FFMA up to 32 Mi MACs
+constexpr int64_t kDefaultSuper = 4096;                 // super-tile edge (raster group)
+// K blocks (of 32) summed in TMEM before the partial sum is added into fp32
+// registers with round-to-nearest adds: 8 blocks = K of 256.
+constexpr int kPromoteBlocks = 8;
+
+std::mutex g_mutex;       // planner caches, device state, workspaces
+std::mutex g_host_mutex;  // serialises the host-buffer entry point (shared staging)
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  int *err = nullptr;  // device status word
+};
+std::map<int, DeviceState> g_devices;
+
+struct Buffer {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+};
+// workspace per (device, stream)
+std::map<std::pair<int, uintptr_t>, Buffer> g_workspaces;
+// staging buffers of the host-pointer entry point, per device
+struct Staging {
+  Buffer a, b, c;
+};
+std::map<int, Staging> g_staging;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+std::atomic<uint64_t> g_launches{0};
+cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;  // instrumentation
+
+cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
+cudaError_t mark(cudaEvent_t ev, cudaStream_t stream) {
+  return ev ? cudaEventRecord(ev, stream) : cudaSuccess;
+}
+
+bool env_flag(const char *name) {
+  const char *v = std::getenv(name);
+  return v && v[0] && std::strcmp(v, "0") != 0;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+phobos_status_t device_state(DeviceState **out, int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  DeviceState &st = g_devices[dev];
+  if (!st.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
+    st.supported = (major == 10 && minor == 3);
+    st.checked = true;
+  }
+  if (!st.supported) return PHOBOS_ERR_UNSUPPORTED;
+  if (!st.err) {
+    if (cudaMalloc(&st.err, sizeof(int)) != cudaSuccess) return PHOBOS_ERR_OUT_OF_MEMORY;
+    if (cudaMemset(st.err, 0, sizeof(int)) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  }
+  *out = &st;
+  if (dev_out) *dev_out = dev;
+  return PHOBOS_OK;
+}
+
+phobos_status_t ensure_buffer(Buffer &b, size_t bytes, cudaStream_t stream) {
+  if (b.bytes >= bytes && b.ptr) return PHOBOS_OK;
+  if (b.ptr) {
+    // stream-ordered: work already enqueued on `stream` keeps the old buffer
+    if (cudaFreeAsync(b.ptr, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+    b.ptr = nullptr;
+    b.bytes = 0;
+  }
+  void *p = nullptr;
+  if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return PHOBOS_ERR_OUT_OF_MEMORY;
+  }
+  b.ptr = p;
+  b.bytes = bytes;
+  return PHOBOS_OK;
+}
+
+phobos_status_t get_encoder() {
+  if (g_encode) return PHOBOS_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return PHOBOS_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return PHOBOS_OK;
+}
+
+// Tensor map of a K-major buffer [rows][kp] fp32, boxes of 32 x box_rows, 128B swizzle.
+phobos_status_t make_kmajor_map(CUtensorMap *map, const float *base, int64_t rows, int64_t kp,
+                                int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kp) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PHOBOS_OK : PHOBOS_ERR_CUDA;
+}
+
+phobos_status_t check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                            int64_t ldc) {
+  if (M < 0 || N < 0 || K < 0) return PHOBOS_ERR_INVALID_VALUE;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return PHOBOS_ERR_INVALID_VALUE;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return PHOBOS_ERR_UNSUPPORTED;
+  return PHOBOS_OK;
+}
+
+size_t tc_workspace(int64_t M, int64_t N, int64_t K, int bn, int passes) {
+  const int64_t Mp = round_up(M, kTcBM), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
+  const int64_t a = round_up(Mp * Kp * 4, 256), b = round_up(Np * Kp * 4, 256);
+  return static_cast<size_t>((a + b) * (passes == 3 ? 2 : 1));
+}
+
+phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
+                          phobos_gemm_plan_t *p) {
+  std::memset(p, 0, sizeof(*p));
+  int path;
+  switch (math) {
+    case PHOBOS_MATH_FFMA: path = PHOBOS_PATH_FFMA; break;
+    case PHOBOS_MATH_TF32: path = PHOBOS_PATH_TF32; break;
+    case PHOBOS_MATH_3XTF32: path = PHOBOS_PATH_3XTF32; break;
+    case PHOBOS_MATH_DEFAULT: {
+      const double macs = static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+      path = (macs <= static_cast<double>(kFfmaMacLimit) || M < 16 || N < 16) ? PHOBOS_PATH_FFMA
+                                                                               : PHOBOS_PATH_3XTF32;
+      break;
+    }
+    default: return PHOBOS_ERR_INVALID_VALUE;
+  }
+  p->path = path;
+  p->cluster_m = 1;
+  p->cluster_n = 1;
+  p->multicast = 0;
+  p->super_k = K;
+  if (path == PHOBOS_PATH_FFMA) {
+    const int t = (M >= 1024 && N >= 1024) ? 128 : 64;
+    p->tile_m = t;
+    p->tile_n = t;
+    p->tile_k = 8;
+    p->stages = 2;
+    p->super_m = round_up(kDefaultSuper, t);
+    p->super_n = round_up(kDefaultSuper, t);
+    p->workspace_bytes = 0;
+  } else {
+    const int passes = path == PHOBOS_PATH_3XTF32 ? 3 : 1;
+    const int bn = N <= 128 ? 128 : 256;
+    p->tile_m = kTcBM;
+    p->tile_n = bn;
+    p->tile_k = kTcBK;
+    p->stages = tc_max_stages(passes, bn);
+    p->super_m = kDefaultSuper;
+    p->super_n = kDefaultSuper;
+    p->workspace_bytes = tc_workspace(M, N, K, bn, passes);
+  }
+  return PHOBOS_OK;
+}
+
+phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
+                              const phobos_gemm_plan_t &p) {
+  if (math == PHOBOS_MATH_FFMA && p.path != PHOBOS_PATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
+  if (math == PHOBOS_MATH_TF32 && p.path != PHOBOS_PATH_TF32) return PHOBOS_ERR_INVALID_VALUE;
+  if (math == PHOBOS_MATH_3XTF32 && p.path != PHOBOS_PATH_3XTF32) return PHOBOS_ERR_INVALID_VALUE;
+  if (p.cluster_m != 1 || p.cluster_n != 1 || p.multicast != 0) return PHOBOS_ERR_UNSUPPORTED;
+  if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
+  if (p.path == PHOBOS_PATH_FFMA) {
+    if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
+      return PHOBOS_ERR_INVALID_VALUE;
+    if (p.tile_k != 8 || (p.super_k < K && p.super_k % 8 != 0)) return PHOBOS_ERR_INVALID_VALUE;
+  } else if (p.path == PHOBOS_PATH_TF32 || p.path == PHOBOS_PATH_3XTF32) {
+    const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
+    if (p.tile_m != kTcBM || (p.tile_n != 128 && p.tile_n != 256) || p.tile_k != kTcBK)
+      return PHOBOS_ERR_INVALID_VALUE;
+    if (p.stages < 2 || p.stages > tc_max_stages(passes, p.tile_n)) return PHOBOS_ERR_INVALID_VALUE;
+    if (p.super_k < K && p.super_k % kTcBK != 0) return PHOBOS_ERR_INVALID_VALUE;
+    if (round_up(N, p.tile_n) / 32 > 65535) return PHOBOS_ERR_UNSUPPORTED;
+  } else {
+    return PHOBOS_ERR_INVALID_VALUE;
+  }
+  return PHOBOS_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+phobos_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PHOBOS_OK;
+  if (e == cudaErrorMemoryAllocation) return PHOBOS_ERR_OUT_OF_MEMORY;
+  return PHOBOS_ERR_CUDA;
+}
+
+void log_plan(int64_t M, int64_t N, int64_t K, const phobos_gemm_plan_t &p) {
+  std::fprintf(stderr,
+               "[phobos] M=%lld N=%lld K=%lld path=%d tile=%dx%dx%d cluster=%dx%d stages=%d "
+               "super=%lldx%lldx%lld workspace=%zu\n",
+               (long long)M, (long long)N, (long long)K, p.path, p.tile_m, p.tile_n, p.tile_k,
+               p.cluster_m, p.cluster_n, p.stages, (long long)p.super_m, (long long)p.super_n,
+               (long long)p.super_k, p.workspace_bytes);
+}
+
+phobos_status_t run_ffma(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                         int64_t ldc, cudaStream_t stream, const phobos_gemm_plan_t &p) {
+  FfmaArgs a{};
+  a.A = A; a.B = B; a.C = C;
+  a.lda = lda; a.ldb = ldb; a.ldc = ldc;
+  a.M = static_cast<int>(M); a.N = static_cast<int>(N); a.K = static_cast<int>(K);
+  a.tile = p.tile_m;
+  a.vec_a = (lda % 4 == 0) && aligned16(A);
+  a.vec_b = (ldb % 4 == 0) && aligned16(B);
+  a.vec_c = (ldc % 4 == 0) && aligned16(C);
+  if (p.super_k >= K) {
+    a.alpha = alpha; a.beta = beta; a.k_begin = 0; a.k_len = static_cast<int>(K);
+    if (mark(g_ev_start, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+    phobos_status_t st = cuda_status(counted(launch_ffma(a, stream)));
+    if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+    return st;
+  }
+  // cluster split: init leaf, then one step leaf per K chunk with beta = 1
+  phobos_status_t st = cuda_status(counted(launch_scale(C, ldc, a.M, a.N, beta, stream)));
+  if (st == PHOBOS_OK && mark(g_ev_start, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+  for (int64_t k0 = 0; st == PHOBOS_OK && k0 < K; k0 += p.super_k) {
+    a.alpha = alpha; a.beta = 1.0f;
+    a.k_begin = static_cast<int>(k0);
+    a.k_len = static_cast<int>(K - k0 < p.super_k ? K - k0 : p.super_k);
+    st = cuda_status(counted(launch_ffma(a, stream)));
+  }
+  if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+  return st;
+}
+
+phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                       const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                       cudaStream_t stream, const phobos_gemm_plan_t &p, DeviceState &dev,
+                       int device) {
+  const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
+  const int bn = p.tile_n;
+  const int64_t Mp = round_up(M, kTcBM), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
+  const size_t need = tc_workspace(M, N, K, bn, passes);
+  Buffer &ws = g_workspaces[{device, reinterpret_cast<uintptr_t>(stream)}];
+  phobos_status_t st = ensure_buffer(ws, need, stream);
+  if (st != PHOBOS_OK) return st;
+  if ((st = get_encoder()) != PHOBOS_OK) return st;
+
+  char *base = static_cast<char *>(ws.ptr);
+  const int64_t a_bytes = round_up(Mp * Kp * 4, 256), b_bytes = round_up(Np * Kp * 4, 256);
+  float *a_big = reinterpret_cast<float *>(base);
+  float *a_small = passes == 3 ? reinterpret_cast<float *>(base + a_bytes) : nullptr;
+  float *b_big = reinterpret_cast<float *>(base + (passes == 3 ? 2 : 1) * a_bytes);
+  float *b_small = passes == 3 ? reinterpret_cast<float *>(base + 2 * a_bytes + b_bytes) : nullptr;
+
+  st = cuda_status(counted(launch_split_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
+                                     static_cast<int>(Mp), static_cast<int>(Kp), a_big, a_small,
+                                     (lda % 4 == 0) && aligned16(A), stream)));
+  if (st != PHOBOS_OK) return st;
+  st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
+                                             static_cast<int>(Np), static_cast<int>(Kp), b_big,
+                                             b_small, stream)));
+  if (st != PHOBOS_OK) return st;
+
+  TcArgs t{};
+  if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
+  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, bn)) != PHOBOS_OK) return st;
+  if (passes == 3) {
+    if ((st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
+    if ((st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, bn)) != PHOBOS_OK) return st;
+  } else {
+    t.tmap_as = t.tmap_ab;
+    t.tmap_bs = t.tmap_bb;
+  }
+  t.C = C;
+  t.ldc = ldc;
+  t.M = static_cast<int>(M);
+  t.N = static_cast<int>(N);
+  t.tiles_m = static_cast<int>(Mp / kTcBM);
+  t.tiles_n = static_cast<int>(Np / bn);
+  int64_t gm = p.super_m / kTcBM;
+  if (gm < 1) gm = 1;
+  if (gm > t.tiles_m) gm = t.tiles_m;
+  t.group_m = static_cast<int>(gm);
+  t.vec_c = (ldc % 4 == 0) && aligned16(C);
+  t.promote_blocks = kPromoteBlocks;
+  t.err = dev.err;
+  const int total_blocks = static_cast<int>(Kp / kTcBK);
+  if (p.super_k >= K) {
+    t.alpha = alpha;
+    t.beta = beta;
+    t.k_block0 = 0;
+    t.k_blocks = total_blocks;
+    if (mark(g_ev_start, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+    st = cuda_status(counted(launch_tc(t, passes, bn, p.stages, stream)));
+    if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+    return st;
+  }
+  // cluster split: init leaf C = beta*C, then step leaves C += alpha * A_c B_c
+  st = cuda_status(counted(launch_scale(C, ldc, t.M, t.N, beta, stream)));
+  if (st == PHOBOS_OK && mark(g_ev_start, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+  const int chunk_blocks = static_cast<int>(p.super_k / kTcBK);
+  for (int kb = 0; st == PHOBOS_OK && kb < total_blocks; kb += chunk_blocks) {
+    t.alpha = alpha;
+    t.beta = 1.0f;
+    t.k_block0 = kb;
+    t.k_blocks = total_blocks - kb < chunk_blocks ? total_blocks - kb : chunk_blocks;
+    st = cuda_status(counted(launch_tc(t, passes, bn, p.stages, stream)));
+  }
+  if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+  return st;
+}
+
+phobos_status_t read_status_word(DeviceState &dev, cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, dev.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PHOBOS_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(dev.err, 0, sizeof(int)) != cudaSuccess) return PHOBOS_ERR_CUDA;
+    if (env_flag("PHOBOS_LOG")) std::fprintf(stderr, "[phobos] device status word 0x%x\n", word);
+    return PHOBOS_ERR_TIMEOUT;
+  }
+  return PHOBOS_OK;
+}
+
+phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                           int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                           int64_t ldc, void *stream_ptr, phobos_math_t math,
+                           const phobos_gemm_plan_t *user_plan) {
+  phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
+  if (st != PHOBOS_OK) return st;
+  if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return PHOBOS_OK;
+  if (!C) return PHOBOS_ERR_INVALID_VALUE;
+  const bool products = K > 0 && alpha != 0.0f;
+  if (products && (!A || !B)) return PHOBOS_ERR_INVALID_VALUE;
+
+  phobos_gemm_plan_t plan;
+  if (user_plan) {
+    plan = *user_plan;
+    if ((st = validate_plan(M, N, K, math, plan)) != PHOBOS_OK) return st;
+  } else if ((st = make_plan(M, N, K, math, &plan)) != PHOBOS_OK) {
+    return st;
+  }
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState *dev = nullptr;
+  int device = 0;
+  if ((st = device_state(&dev, &device)) != PHOBOS_OK) return st;
+  if (env_flag("PHOBOS_LOG")) log_plan(M, N, K, plan);
+
+  if (!products) {
+    st = cuda_status(counted(launch_scale(C, ldc, static_cast<int>(M), static_cast<int>(N), beta, stream)));
+  } else if (plan.path == PHOBOS_PATH_FFMA) {
+    st = run_ffma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan);
+  } else {
+    st = run_tc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev, device);
+  }
+  if (st == PHOBOS_OK && env_flag("PHOBOS_DEBUG_SYNC")) st = read_status_word(*dev, stream);
+  return st;
+}
+
+}  // namespace
+}  // namespace phobos
+
+using namespace phobos;
+
+extern "C" {
+
+phobos_status_t phobos_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t ldc, phobos_math_t math, phobos_gemm_plan_t *out) {
+  if (!out) return PHOBOS_ERR_INVALID_VALUE;
+  phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
+  if (st == PHOBOS_ERR_UNSUPPORTED) return st;
+  if (st != PHOBOS_OK) return st;
+  return make_plan(M, N, K, math, out);
+}
+
+phobos_status_t phobos_sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                             int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                             int64_t ldc, void *stream) {
+  return sgemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, PHOBOS_MATH_DEFAULT,
+                    nullptr);
+}
+
+phobos_status_t phobos_sgemm_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                                int64_t ldc, void *stream, phobos_math_t math,
+                                const phobos_gemm_plan_t *plan) {
+  return sgemm_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, math, plan);
+}
+
+phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                  int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                                  int64_t ldc, void *stream_ptr, phobos_math_t math) {
+  phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
+  if (st != PHOBOS_OK) return st;
+  if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return PHOBOS_OK;
+  if (!C) return PHOBOS_ERR_INVALID_VALUE;
+  const bool products = K > 0 && alpha != 0.0f;
+  if (products && (!A || !B)) return PHOBOS_ERR_INVALID_VALUE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  std::lock_guard<std::mutex> host_lock(g_host_mutex);
+  // extents of the strided host arrays, in elements
+  const size_t a_elems = products ? static_cast<size_t>((M - 1) * lda + K) : 0;
+  const size_t b_elems = products ? static_cast<size_t>((K - 1) * ldb + N) : 0;
+  const size_t c_elems = static_cast<size_t>((M - 1) * ldc + N);
+  float *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *dev = nullptr;
+    int device = 0;
+    if ((st = device_state(&dev, &device)) != PHOBOS_OK) return st;
+    Staging &s = g_staging[device];
+    if (products && (st = ensure_buffer(s.a, a_elems * 4, stream)) != PHOBOS_OK) return st;
+    if (products && (st = ensure_buffer(s.b, b_elems * 4, stream)) != PHOBOS_OK) return st;
+    if ((st = ensure_buffer(s.c, c_elems * 4, stream)) != PHOBOS_OK) return st;
+    dA = static_cast<float *>(s.a.ptr);
+    dB = static_cast<float *>(s.b.ptr);
+    dC = static_cast<float *>(s.c.ptr);
+  }
+  if (products) {
+    if (cudaMemcpyAsync(dA, A, a_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dB, B, b_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
+  }
+  if (beta != 0.0f &&
+      cudaMemcpyAsync(dC, C, c_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return PHOBOS_ERR_CUDA;
+  st = sgemm_impl(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, stream_ptr, math, nullptr);
+  if (st != PHOBOS_OK) return st;
+  if (cudaMemcpyAsync(C, dC, c_elems * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PHOBOS_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  return PHOBOS_OK;
+}
+
+phobos_status_t phobos_check_device(void *stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState *dev = nullptr;
+  phobos_status_t st = device_state(&dev, nullptr);
+  if (st != PHOBOS_OK) return st;
+  return read_status_word(*dev, static_cast<cudaStream_t>(stream));
+}
+
+phobos_status_t phobos_set_timing_events(void *start, void *stop) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_ev_start = static_cast<cudaEvent_t>(start);
+  g_ev_stop = static_cast<cudaEvent_t>(stop);
+  return PHOBOS_OK;
+}
+
+uint64_t phobos_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+phobos_status_t phobos_release(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int current = 0;
+  if (cudaGetDevice(&current) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  phobos_status_t st = PHOBOS_OK;
+  auto free_on = [&](int device, Buffer &b) {
+    if (!b.ptr) return;
+    if (cudaSetDevice(device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaFree(b.ptr) != cudaSuccess)
+      st = PHOBOS_ERR_CUDA;
+    b.ptr = nullptr;
+    b.bytes = 0;
+  };
+  for (auto &kv : g_workspaces) free_on(kv.first.first, kv.second);
+  g_workspaces.clear();
+  for (auto &kv : g_staging) {
+    free_on(kv.first, kv.second.a);
+    free_on(kv.first, kv.second.b);
+    free_on(kv.first, kv.second.c);
+  }
+  g_staging.clear();
+  cudaSetDevice(current);
+  return st;
+}
+
+const char *phobos_status_string(phobos_status_t status) {
+  switch (status) {
+    case PHOBOS_OK: return "PHOBOS_OK: success";
+    case PHOBOS_ERR_INVALID_VALUE: return "PHOBOS_ERR_INVALID_VALUE: invalid argument or plan";
+    case PHOBOS_ERR_UNSUPPORTED: return "PHOBOS_ERR_UNSUPPORTED: device or shape not supported";
+    case PHOBOS_ERR_CUDA: return "PHOBOS_ERR_CUDA: a CUDA call failed";
+    case PHOBOS_ERR_OUT_OF_MEMORY: return "PHOBOS_ERR_OUT_OF_MEMORY: workspace allocation failed";
+    case PHOBOS_ERR_TIMEOUT: return "PHOBOS_ERR_TIMEOUT: a device-side bounded wait expired";
+  }
+  return "unknown phobos status";
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+// Register-tiled fp32 SGEMM on the CUDA cores (fused multiply-add), for small
+// problems and for callers who ask for plain fp32 products.
+//
+// This is the pages' own fp32 path ("Show HN: Phobos", "GPU Performance"):
+// coalesced global loads, a shared-memory tile per CTA, a per-thread register
+// micro-tile (8 x 8 outputs) read from shared memory without bank conflicts,
+// and ping-pong buffering of the K tiles ("Are we cuBLAS yet?": ping-pong
+// buffering and pipelining).  The CTA tile is 128 x 128 x 8 (256 threads) or
+// 64 x 64 x 8 (64 threads); the pages' tuned winner on their GPU was
+// 64 x 128 x 8.  Any M, N, K and leading dimension is accepted: loads outside
+// the matrix read zero and stores outside it are skipped.
+#include "internal.h"
+
+namespace phobos {
+
+namespace {
+
+constexpr int kBK = 8;
+
+template <int BM, int BN>
+__global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const FfmaArgs p) {
+  constexpr int NT = (BM / 8) * (BN / 8);
+  constexpr int PAD = 4;
+  constexpr int A_LOADS = BM * kBK / 4 / NT;  // float4 groups of A per thread
+  constexpr int B_LOADS = BN * kBK / 4 / NT;  // float4 groups of B per thread
+  static_assert(A_LOADS >= 1 && B_LOADS >= 1, "tile too small for the thread count");
+  __shared__ __align__(16) float As[2][kBK][BM + PAD];
+  __shared__ __align__(16) float Bs[2][kBK][BN + PAD];
+
+  const int tid = threadIdx.x;
+  const int tiles_n = (p.N + BN - 1) / BN;
+  const int tm = blockIdx.x / tiles_n;
+  const int tn = blockIdx.x - tm * tiles_n;
+  const int m0 = tm * BM, n0 = tn * BN;
+  const int tx = tid % (BN / 8);
+  const int ty = tid / (BN / 8);
+
+  float a_reg[A_LOADS][4];
+  float b_reg[B_LOADS][4];
+
+  auto load_tiles = [&](int k0) {
+#pragma unroll
+    for (int l = 0; l < A_LOADS; ++l) {
+      const int g = tid + l * NT;       // group index in the BM x 8 tile
+      const int row = g / (kBK / 4);
+      const int kq = (g % (kBK / 4)) * 4;
+      const int gi = m0 + row, gk = k0 + kq;
+      const float *src = p.A + static_cast<int64_t>(gi) * p.lda + gk;
+      if (gi < p.M && p.vec_a && gk + 3 < p.k_begin + p.k_len) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+        a_reg[l][0] = v.x; a_reg[l][1] = v.y; a_reg[l][2] = v.z; a_reg[l][3] = v.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          a_reg[l][t] = (gi < p.M && gk + t < p.k_begin + p.k_len) ? __ldg(src + t) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int l = 0; l < B_LOADS; ++l) {
+      const int g = tid + l * NT;       // group index in the 8 x BN tile
+      const int k = g / (BN / 4);
+      const int nq = (g % (BN / 4)) * 4;
+      const int gk = k0 + k, gj = n0 + nq;
+      const float *src = p.B + static_cast<int64_t>(gk) * p.ldb + gj;
+      const bool krow = gk < p.k_begin + p.k_len;
+      if (krow && p.vec_b && gj + 3 < p.N) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+        b_reg[l][0] = v.x; b_reg[l][1] = v.y; b_reg[l][2] = v.z; b_reg[l][3] = v.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) b_reg[l][t] = (krow && gj + t < p.N) ? __ldg(src + t) : 0.f;
+      }
+    }
+  };
+
+  auto store_tiles = [&](int buf) {
+#pragma unroll
+    for (int l = 0; l < A_LOADS; ++l) {
+      const int g = tid + l * NT;
+      const int row = g / (kBK / 4);
+      const int kq = (g % (kBK / 4)) * 4;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) As[buf][kq + t][row] = a_reg[l][t];
+    }
+#pragma unroll
+    for (int l = 0; l < B_LOADS; ++l) {
+      const int g = tid + l * NT;
+      const int k = g / (BN / 4);
+      const int nq = (g % (BN / 4)) * 4;
+      *reinterpret_cast<float4 *>(&Bs[buf][k][nq]) =
+          make_float4(b_reg[l][0], b_reg[l][1], b_reg[l][2], b_reg[l][3]);
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  const int k_end = p.k_begin + p.k_len;
+  int buf = 0;
+  load_tiles(p.k_begin);
+  store_tiles(0);
+  __syncthreads();
+  for (int k0 = p.k_begin; k0 < k_end; k0 += kBK) {
+    const bool more = k0 + kBK < k_end;
+    if (more) load_tiles(k0 + kBK);  // global loads in flight during the FMAs
+#pragma unroll
+    for (int k = 0; k < kBK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][ty * 4 + BM / 2]);
+      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][tx * 4 + BN / 2]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (more) {
+      store_tiles(buf ^ 1);
+      __syncthreads();
+      buf ^= 1;
+    }
+  }
+
+  // Epilogue: C = alpha * acc + beta * C_old; beta == 0 does not read C.
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+    if (row >= p.M) continue;
+    float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int col = n0 + tx * 4 + h * (BN / 2);
+      if (p.vec_c && col + 3 < p.N) {
+        float4 *dst = reinterpret_cast<float4 *>(crow + col);
+        float4 o;
+        if (p.beta != 0.0f) {
+          const float4 old = *dst;
+          o.x = fmaf(p.alpha, acc[i][4 * h + 0], p.beta * old.x);
+          o.y = fmaf(p.alpha, acc[i][4 * h + 1], p.beta * old.y);
+          o.z = fmaf(p.alpha, acc[i][4 * h + 2], p.beta * old.z);
+          o.w = fmaf(p.alpha, acc[i][4 * h + 3], p.beta * old.w);
+        } else {
+          o.x = p.alpha * acc[i][4 * h + 0];
+          o.y = p.alpha * acc[i][4 * h + 1];
+          o.z = p.alpha * acc[i][4 * h + 2];
+          o.w = p.alpha * acc[i][4 * h + 3];
+        }
+        *dst = o;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (col + t < p.N) {
+            const float v = acc[i][4 * h + t];
+            crow[col + t] = p.beta != 0.0f ? fmaf(p.alpha, v, p.beta * crow[col + t]) : p.alpha * v;
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ffma(const FfmaArgs &a, cudaStream_t stream) {
+  if (a.tile == 128) {
+    const int64_t tiles = static_cast<int64_t>((a.M + 127) / 128) * ((a.N + 127) / 128);
+    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    sgemm_ffma_kernel<128, 128><<<static_cast<unsigned>(tiles), 256, 0, stream>>>(a);
+  } else if (a.tile == 64) {
+    const int64_t tiles = static_cast<int64_t>((a.M + 63) / 64) * ((a.N + 63) / 64);
+    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    sgemm_ffma_kernel<64, 64><<<static_cast<unsigned>(tiles), 64, 0, stream>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace phobos

@@ -1,0 +1,332 @@
+// Tensor-core SGEMM for sm_103a: C = alpha * A * B + beta * C on the
+// fifth-generation tensor cores, with operands split into tf32 pairs.
+//
+// What is computed (the accumulator-tile kernel of the "@cluster" attribute
+// page, `matmul` listing; "Show HN: Phobos", "Matrix Multiplication"): one CTA
+// owns a 128 x BN tile of C, loops over K in blocks of 32, accumulates
+// acc += A[tile rows, k block] * B[k block, tile cols], and stores
+// alpha * acc + beta * C_old once at the end.
+//
+// How it maps onto GB300:
+//  - Operand K-panels arrive by TMA into an S-stage shared-memory ring with
+//    128-byte swizzling, gated by full/empty mbarriers (the pages' "@pipeline"
+//    ping-pong buffering, generalised to S stages).
+//  - One thread issues tcgen05.mma (kind::tf32, M = 128, N = BN, K = 8) into a
+//    tensor-memory (TMEM) accumulator; a commit to the stage's empty barrier
+//    releases the slot to the producer.
+//  - Split TF32 (passes = 3): a = a_big + a_small with both parts rounded to
+//    tf32 by the pre-pass, and acc += a_small*b_big + a_big*b_small +
+//    a_big*b_big per K = 8 slice; the dropped a_small*b_small term is below
+//    2^-22 |a||b|.  passes = 1 issues a_big*b_big only.
+//  - Promotion: the tensor core's fp32 accumulation rounds towards zero, which
+//    biases long sums (measured on GB300: at K = 8192 the split-TF32 error
+//    reached 3.7e-6 of sum|a||b| for random signs, and a -8.6e-5 mean bias for
+//    positive data).  So TMEM only holds a partial sum over `promote_blocks`
+//    K blocks (default 8, i.e. K = 256).  Two TMEM buffers alternate: while
+//    the MMAs fill one, eight epilogue warps read the other with tcgen05.ld and
+//    add it into fp32 registers with round-to-nearest adds.  This is the
+//    remedy of Ootomo & Yokota (2022) for tensor-core accumulation, done with
+//    TMEM double buffering.  The tile's final sum therefore lives in registers
+//    (128 lanes x BN columns spread over 256 threads), the same place the
+//    pages' codegen puts a CTA-wide accumulator tile.
+//  - Epilogue: fmaf(alpha, sum, beta * c_old) with 16-byte vector loads and
+//    stores where C allows and scalar edge handling.
+//
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
+// MMA issuer, warps 2..9 = accumulator/epilogue warps.  Epilogue warp w reads
+// TMEM lanes 32*(w%4) .. +31 (the hardware's lane-quarter rule) and columns
+// [h*BN/2, (h+1)*BN/2) with h = (w-2)/4.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace phobos {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 32;  // fp32 elements per row of one stage = 128 bytes = swizzle span
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSmemLimit = 227 * 1024;
+
+template <int BN, int PASSES>
+struct TcShape {
+  static constexpr int kOps = PASSES == 3 ? 2 : 1;  // big (+ small) per operand
+  static constexpr int kATile = kBM * kBK * 4;       // 16 KiB
+  static constexpr int kBTile = BN * kBK * 4;
+  static constexpr int kStageBytes = kOps * (kATile + kBTile);
+  static constexpr int kTmemCols = 2 * BN;           // two accumulator buffers
+  static constexpr int kAux = 1024 + 256;            // alignment slack + barriers
+  static constexpr int max_stages() { return (kSmemLimit - kAux) / kStageBytes; }
+  static constexpr int smem_bytes(int stages) { return stages * kStageBytes + kAux; }
+};
+
+__device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group_m, int &tm,
+                                       int &tn) {
+  // Output tiles are walked super-tile by super-tile: group_m tile rows at a
+  // time, column by column inside the group, so that the CTAs resident at one
+  // time share A row panels and B column panels in L2.
+  const int per_group = group_m * tiles_n;
+  const int g = t / per_group;
+  const int first = g * group_m;
+  const int rows = min(group_m, tiles_m - first);
+  const int r = t - g * per_group;
+  tm = first + r % rows;
+  tn = r / rows;
+}
+
+template <int BN, int PASSES, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
+  using S = TcShape<BN, PASSES>;
+  constexpr int kHalf = BN / 2;  // columns summed by one epilogue thread
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t tiles = (raw + 1023u) & ~1023u;  // 1024-byte aligned stage ring
+  uint8_t *aux = smem_raw + (tiles - raw) + STAGES * S::kStageBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(aux);
+  // bars: [0,S) full, [S,2S) empty, 2S+{0,1} acc_full, 2S+{2,3} acc_empty, 2S+4 MMA drained
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * STAGES;
+  const uint32_t acc_full0 = full0 + 16u * STAGES;
+  const uint32_t acc_empty0 = acc_full0 + 16u;
+  const uint32_t mma_drained = acc_full0 + 32u;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int tm, tn;
+  raster(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  const int m0 = tm * kBM;
+  const int n0 = tn * BN;
+  const int chunk = p.promote_blocks;
+  const int n_chunks = (p.k_blocks + chunk - 1) / chunk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full0 + 8u * b, 1);
+      mbar_init(acc_empty0 + 8u * b, kEpiWarps);
+    }
+    mbar_init(mma_drained, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tmap_ab);
+    prefetch_tmap(&p.tmap_bb);
+    if (PASSES == 3) {
+      prefetch_tmap(&p.tmap_as);
+      prefetch_tmap(&p.tmap_bs);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t armed = 0, last_parity = 0;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1u;
+        if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) break;
+        const uint32_t full = full0 + 8u * s;
+        mbar_arrive_expect_tx(full, S::kStageBytes);
+        const int kc = (p.k_block0 + kb) * kBK;
+        const uint32_t st = tiles + s * S::kStageBytes;
+        tma_load_2d(st, &p.tmap_ab, full, kc, m0);
+        if (PASSES == 3) tma_load_2d(st + S::kATile, &p.tmap_as, full, kc, m0);
+        const uint32_t bt = st + S::kOps * S::kATile;
+        tma_load_2d(bt, &p.tmap_bb, full, kc, n0);
+        if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, n0);
+        armed |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+      }
+      // No bulk copy may still be writing this CTA's shared memory at exit.
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s))
+          bounded_wait(full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
+                       kDevTimeoutDrain, false);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(kBM, BN);
+      int kb = 0;
+      bool ok = true;
+      for (int c = 0; c < n_chunks && ok; ++c) {
+        const int b = c & 1;
+        const uint32_t use = static_cast<uint32_t>(c >> 1);
+        // the epilogue warps must have read this buffer's previous partial sum
+        if (!bounded_wait(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
+                          kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        const int kb_end = min(p.k_blocks, kb + chunk);
+        for (int first = 1; kb < kb_end; ++kb, first = 0) {
+          const int s = kb % STAGES;
+          const uint32_t ph = (kb / STAGES) & 1u;
+          if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_big = tiles + s * S::kStageBytes;
+          const uint32_t a_small = a_big + S::kATile;
+          const uint32_t b_big = a_big + S::kOps * S::kATile;
+          const uint32_t b_small = b_big + S::kBTile;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 8; ++kk) {
+            const uint32_t off = kk * 32u;  // 8 tf32 = 32 bytes along K
+            const uint64_t dab = desc_kmajor_sw128(a_big + off);
+            const uint64_t dbb = desc_kmajor_sw128(b_big + off);
+            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+            if (PASSES == 3) {
+              const uint64_t das = desc_kmajor_sw128(a_small + off);
+              const uint64_t dbs = desc_kmajor_sw128(b_small + off);
+              mma_tf32(d_tmem, das, dbb, idesc, acc);
+              mma_tf32(d_tmem, dab, dbs, idesc, 1u);
+              mma_tf32(d_tmem, dab, dbb, idesc, 1u);
+            } else {
+              mma_tf32(d_tmem, dab, dbb, idesc, acc);
+            }
+          }
+          mma_commit(empty0 + 8u * s);
+        }
+        if (ok) mma_commit(acc_full0 + 8u * b);
+      }
+      // Every MMA must be finished before TMEM is released.
+      mma_commit(mma_drained);
+      bounded_wait(mma_drained, 0, abort_flag, p.err, kDevTimeoutDrain, false);
+    }
+  } else {
+    // ------------------------------------------- accumulate + epilogue warps
+    const int q = warp & 3;              // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;       // column half
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float sum[kHalf];
+#pragma unroll
+    for (int j = 0; j < kHalf; ++j) sum[j] = 0.f;
+    bool ok = true;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int b = c & 1;
+      const uint32_t use = static_cast<uint32_t>(c >> 1);
+      if (!bounded_wait(acc_full0 + 8u * b, use & 1u, abort_flag, p.err, kDevTimeoutEpilogue)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t col = tmem_base + static_cast<uint32_t>(b * BN + h * kHalf);
+#pragma unroll
+      for (int j = 0; j < kHalf; j += 32) {
+        uint32_t r[32];
+        tmem_ld32(col + lane_base + j, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) sum[j + t] = __fadd_rn(sum[j + t], __uint_as_float(r[t]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty0 + 8u * b);
+    }
+    if (ok) {
+      const int row = m0 + q * 32 + lane;
+      const int col0 = n0 + h * kHalf;
+      if (row < p.M && col0 < p.N) {
+        float *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+        const float alpha = p.alpha, beta = p.beta;
+        if (p.vec_c && col0 + kHalf <= p.N) {
+          float4 *dst = reinterpret_cast<float4 *>(crow);
+#pragma unroll
+          for (int v = 0; v < kHalf / 4; ++v) {
+            float4 o;
+            if (beta != 0.0f) {
+              const float4 old = dst[v];
+              o.x = fmaf(alpha, sum[4 * v + 0], beta * old.x);
+              o.y = fmaf(alpha, sum[4 * v + 1], beta * old.y);
+              o.z = fmaf(alpha, sum[4 * v + 2], beta * old.z);
+              o.w = fmaf(alpha, sum[4 * v + 3], beta * old.w);
+            } else {
+              o.x = alpha * sum[4 * v + 0];
+              o.y = alpha * sum[4 * v + 1];
+              o.z = alpha * sum[4 * v + 2];
+              o.w = alpha * sum[4 * v + 3];
+            }
+            dst[v] = o;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kHalf; ++j) {
+            if (col0 + j < p.N)
+              crow[j] = beta != 0.0f ? fmaf(alpha, sum[j], beta * crow[j]) : alpha * sum[j];
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+template <int BN, int PASSES, int STAGES>
+cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
+  using S = TcShape<BN, PASSES>;
+  static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES>;
+  const int smem = S::smem_bytes(STAGES);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(a.tiles_m) * static_cast<unsigned>(a.tiles_n);
+  kern<<<grid, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int BN, int PASSES>
+cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream) {
+  constexpr int kMax = TcShape<BN, PASSES>::max_stages();
+  if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2)>(a, stream);
+  if (stages >= 3 && kMax >= 3) return launch_one<BN, PASSES, (kMax >= 3 ? 3 : 2)>(a, stream);
+  if (stages >= 2) return launch_one<BN, PASSES, 2>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int tc_max_stages(int passes, int bn) {
+  int m = 0;
+  if (passes == 3 && bn == 256) m = TcShape<256, 3>::max_stages();
+  if (passes == 3 && bn == 128) m = TcShape<128, 3>::max_stages();
+  if (passes == 1 && bn == 256) m = TcShape<256, 1>::max_stages();
+  if (passes == 1 && bn == 128) m = TcShape<128, 1>::max_stages();
+  return m > 4 ? 4 : m;
+}
+
+cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream) {
+  if (passes == 3 && bn == 256) return launch_stages<256, 3>(a, stages, stream);
+  if (passes == 3 && bn == 128) return launch_stages<128, 3>(a, stages, stream);
+  if (passes == 1 && bn == 256) return launch_stages<256, 1>(a, stages, stream);
+  if (passes == 1 && bn == 128) return launch_stages<128, 1>(a, stages, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace phobos

@@ -1,0 +1,125 @@
+// Operand pre-pass of the tensor-core path and the beta-scaling leaf.
+//
+// Split TF32: every fp32 operand value x is written as two tf32 values,
+//   big = rna_tf32(x),  small = rna_tf32(x - big)
+// (x - big is exact in fp32), so x = big + small up to 2^-22 |x|.  Both are
+// stored as 32-bit containers whose low 13 bits are zero, in K-major buffers
+// padded with zeros to whole tiles: A stays row-major [Mp][Kp], B is
+// transposed to [Np][Kp].  Padded rows and the K tail are zero, so the main
+// kernel never needs bounds checks on its operands and TMA boxes never leave
+// the buffers.  The pages convert fp32 operands before the tensor cores too,
+// and note the single conversion is lossy ("Show HN: Phobos", footnote 14);
+// the two-term split recovers fp32-level products.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace phobos {
+
+namespace {
+
+__global__ void __launch_bounds__(256) split_rows_kernel(const float *__restrict__ A, int64_t lda,
+                                                         int M, int K, int Mp, int Kp,
+                                                         float *__restrict__ big,
+                                                         float *__restrict__ small, int vec) {
+  const int64_t groups_per_row = Kp / 4;
+  const int64_t total = static_cast<int64_t>(Mp) * groups_per_row;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(g / groups_per_row);
+    const int k = static_cast<int>(g - static_cast<int64_t>(i) * groups_per_row) * 4;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < M) {
+      const float *src = A + static_cast<int64_t>(i) * lda + k;
+      if (vec && k + 3 < K) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (k + t < K) x[t] = __ldg(src + t);
+      }
+    }
+    float4 b, s;
+    b.x = to_tf32_rna(x[0]); s.x = to_tf32_rna(x[0] - b.x);
+    b.y = to_tf32_rna(x[1]); s.y = to_tf32_rna(x[1] - b.y);
+    b.z = to_tf32_rna(x[2]); s.z = to_tf32_rna(x[2] - b.z);
+    b.w = to_tf32_rna(x[3]); s.w = to_tf32_rna(x[3] - b.w);
+    const int64_t o = static_cast<int64_t>(i) * Kp + k;
+    *reinterpret_cast<float4 *>(big + o) = b;
+    if (small) *reinterpret_cast<float4 *>(small + o) = s;
+  }
+}
+
+// B (K x N) -> K-major [Np][Kp] through a 32 x 32 shared-memory tile.
+__global__ void __launch_bounds__(256) split_cols_kernel(const float *__restrict__ B, int64_t ldb,
+                                                         int K, int N, int Kp,
+                                                         float *__restrict__ big,
+                                                         float *__restrict__ small) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32;
+  const int n0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;  // 0..7
+#pragma unroll
+  for (int r = 0; r < 32; r += 8) {
+    const int k = k0 + ty + r;
+    const int n = n0 + tx;
+    tile[ty + r][tx] = (k < K && n < N) ? __ldg(B + static_cast<int64_t>(k) * ldb + n) : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 32; r += 8) {
+    const int n = n0 + ty + r;
+    const int k = k0 + tx;
+    const float x = tile[tx][ty + r];
+    const float b = to_tf32_rna(x);
+    const int64_t o = static_cast<int64_t>(n) * Kp + k;
+    big[o] = b;
+    if (small) small[o] = to_tf32_rna(x - b);
+  }
+}
+
+__global__ void __launch_bounds__(256) scale_kernel(float *C, int64_t ldc, int M, int N,
+                                                    float beta) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t i = e / N;
+    const int64_t j = e - i * N;
+    float *c = C + i * ldc + j;
+    *c = beta == 0.0f ? 0.0f : beta * *c;
+  }
+}
+
+unsigned grid_for(int64_t work, int per_block) {
+  int64_t blocks = (work + per_block - 1) / per_block;
+  // enough blocks to fill every SM several times; the kernels stride the rest
+  const int64_t cap = 152 * 32;
+  if (blocks > cap) blocks = cap;
+  return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_split_rows(const float *A, int64_t lda, int M, int K, int Mp, int Kp,
+                              float *big, float *small, int vec, cudaStream_t stream) {
+  const int64_t groups = static_cast<int64_t>(Mp) * (Kp / 4);
+  split_rows_kernel<<<grid_for(groups, 256), 256, 0, stream>>>(A, lda, M, K, Mp, Kp, big, small,
+                                                               vec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_cols(const float *B, int64_t ldb, int K, int N, int Np, int Kp,
+                              float *big, float *small, cudaStream_t stream) {
+  dim3 grid(Kp / 32, Np / 32);
+  split_cols_kernel<<<grid, 256, 0, stream>>>(B, ldb, K, N, Kp, big, small);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  scale_kernel<<<grid_for(total, 256), 256, 0, stream>>>(C, ldc, M, N, beta);
+  return cudaGetLastError();
+}
+
+}  // namespace phobos

@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, validates arguments and plans without touching a GPU."""
+import os
+import re
+import subprocess
+
+import pytest
+
+import language_fp32_gemm_gb300 as phobos
+from language_fp32_gemm_gb300 import build as lib_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "phobos_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return phobos.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(phobos_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(phobos.ABI_FUNCTIONS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", phobos.LIBRARY_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert phobos.status_string(code).startswith("PHOBOS_")
+    assert "unknown" in phobos.status_string(99)
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, 4, 4, 4),      # negative M
+    (4, -1, 4, 4, 4, 4),      # negative N
+    (4, 4, -1, 4, 4, 4),      # negative K
+    (4, 4, 8, 7, 4, 4),       # lda < K
+    (4, 8, 4, 4, 7, 8),       # ldb < N
+    (4, 8, 4, 4, 8, 7),       # ldc < N
+])
+def test_invalid_sizes_rejected_before_any_device_call(lib, args):
+    M, N, K, lda, ldb, ldc = args
+    st = phobos.phobos_sgemm(M, N, K, 1.0, 16, lda, 16, ldb, 0.0, 16, ldc, 0)
+    assert st == phobos.PHOBOS_ERR_INVALID_VALUE
+    with pytest.raises(phobos.PhobosError):
+        phobos.phobos_gemm_plan(M, N, K, lda, ldb, ldc)
+
+
+def test_null_pointers_rejected(lib):
+    assert phobos.phobos_sgemm(4, 4, 4, 1.0, 0, 4, 16, 4, 0.0, 16, 4, 0) == phobos.PHOBOS_ERR_INVALID_VALUE
+    assert phobos.phobos_sgemm(4, 4, 4, 1.0, 16, 4, 0, 4, 0.0, 16, 4, 0) == phobos.PHOBOS_ERR_INVALID_VALUE
+    assert phobos.phobos_sgemm(4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 0, 4, 0) == phobos.PHOBOS_ERR_INVALID_VALUE
+    assert phobos.phobos_sgemm_ex(4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, 0, 7) == phobos.PHOBOS_ERR_INVALID_VALUE
+
+
+def test_empty_output_is_a_no_op(lib):
+    assert phobos.phobos_sgemm(0, 5, 5, 1.0, 0, 5, 0, 5, 0.0, 0, 5, 0) == phobos.PHOBOS_OK
+    assert phobos.phobos_sgemm(5, 0, 5, 1.0, 0, 5, 0, 1, 0.0, 0, 1, 0) == phobos.PHOBOS_OK
+
+
+def test_plan_paths(lib):
+    p = phobos.phobos_gemm_plan(256, 256, 256, 256, 256, 256)
+    assert p.path == phobos.PHOBOS_PATH_FFMA and p.workspace_bytes == 0
+    p = phobos.phobos_gemm_plan(8192, 8192, 8192, 8192, 8192, 8192)
+    assert p.path == phobos.PHOBOS_PATH_3XTF32
+    assert p.tile_m == 128 and p.tile_n == 256 and p.tile_k == 32 and p.stages >= 2
+    assert p.super_k == 8192 and p.super_m == 4096
+    # split operands: (Mp + Np) * Kp * 4 bytes, big and small
+    assert p.workspace_bytes == 2 * (8192 + 8192) * 8192 * 4
+    p = phobos.phobos_gemm_plan(8192, 8192, 8192, 8192, 8192, 8192, "tf32")
+    assert p.path == phobos.PHOBOS_PATH_TF32 and p.workspace_bytes == (8192 + 8192) * 8192 * 4
+    p = phobos.phobos_gemm_plan(3001, 5003, 1999, 1999, 5003, 5003)
+    Mp, Np, Kp = 3072, 5120, 2016
+    assert p.workspace_bytes == 2 * (Mp * Kp * 4 + Np * Kp * 4)
+    p = phobos.phobos_gemm_plan(65536, 256, 4096, 4096, 256, 256)
+    assert p.tile_n == 256
+    p = phobos.phobos_gemm_plan(4096, 100, 4096, 4096, 100, 100)
+    assert p.tile_n == 128
+    p = phobos.phobos_gemm_plan(8, 4096, 4096, 4096, 4096, 4096)
+    assert p.path == phobos.PHOBOS_PATH_FFMA
+
+
+def test_plan_rejects_unknown_math(lib):
+    with pytest.raises(phobos.PhobosError):
+        phobos.phobos_gemm_plan(16, 16, 16, 16, 16, 16, 9)

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bars (on the oracle's error scale den = |alpha| sum|a||b| + |beta||c_old|):
+max |C - C_ref| / den <= 2^-20 for 3xTF32, FFMA and the K-chunked mode and
+<= 2^-10 for single-pass TF32; bit-exact (C == float32(C_ref)) for integer
+inputs and for the B = 0 closed form, in every mode.
+"""
+import numpy as np
+import pytest
+
+import language_fp32_gemm_gb300 as phobos
+import oracle
+import seeded_inputs as si
+from gpu_util import padded, run_gemm, tolerance
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+MATHS = ["default", "3xtf32", "tf32", "ffma"]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from language_fp32_gemm_gb300 import build as lib_build
+    lib_build.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+def check(dev, A, B, C0, alpha, beta, math, plan=None, offsets=(0, 0, 0)):
+    C = run_gemm(torch, dev, A, B, C0, alpha, beta, math, plan=plan, offsets=offsets)
+    ref, den = oracle.sgemm(A, B, C0, alpha, beta)
+    err = oracle.max_rel_error(C, ref, den)
+    assert err <= tolerance(math), "%s: max rel error %.3g" % (math, err)
+    return C, ref, err
+
+
+# ------------------------------------------------------------- config 1: 256^3
+
+@pytest.mark.parametrize("math", MATHS)
+def test_uniform_256(dev, math):
+    w = si.workload("sgemm_256")
+    check(dev, w.A(), w.B(), w.C_old(), w.alpha, w.beta, math)
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_integer_256_bit_exact(dev, math):
+    w = si.workload("sgemm_256_int")
+    A, B, C0 = w.A(), w.B(), w.C_old()
+    C = run_gemm(torch, dev, A, B, C0, w.alpha, w.beta, math)
+    ref, _ = oracle.sgemm(A, B, C0, w.alpha, w.beta)
+    assert np.array_equal(C, oracle.ref32(ref))
+
+
+# ------------------------------------------------------- edges and degenerates
+
+EDGE_SHAPES = [(1, 1, 1), (1, 300, 17), (300, 1, 17), (7, 13, 5), (129, 257, 33),
+               (128, 256, 32), (255, 129, 95), (300, 260, 200), (513, 384, 1000),
+               (16, 520, 64), (130, 17, 260)]
+
+
+@pytest.mark.parametrize("math", ["3xtf32", "tf32", "ffma"])
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "%dx%dx%d" % s)
+def test_edge_shapes(dev, shape, math):
+    M, N, K = shape
+    seed = 1000 + M * 7 + N * 3 + K
+    A = si.normal(seed, 0, (M, K))
+    B = si.normal(seed, 1, (K, N))
+    C0 = si.uniform_pm1(seed, 2, (M, N))
+    check(dev, A, B, C0, 1.25, -0.5, math)
+
+
+@pytest.mark.parametrize("math", ["3xtf32", "tf32", "ffma"])
+def test_padded_leading_dimensions(dev, math):
+    M, N, K = 200, 150, 90
+    A = padded(si.normal(31, 0, (M, K)), 3)
+    B = padded(si.normal(31, 1, (K, N)), 5)
+    C0 = padded(si.uniform_pm1(31, 2, (M, N)), 1)
+    check(dev, A, B, C0, 0.5, 2.0, math)
+
+
+@pytest.mark.parametrize("math", ["3xtf32", "tf32", "ffma"])
+def test_unaligned_pointers(dev, math):
+    M, N, K = 190, 170, 120
+    A = si.normal(32, 0, (M, K))
+    B = si.normal(32, 1, (K, N))
+    C0 = si.uniform_pm1(32, 2, (M, N))
+    check(dev, A, B, C0, 1.0, 0.5, math, offsets=(1, 3, 1))
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_closed_form_zero_b_bit_exact(dev, math):
+    M, N, K = 300, 270, 130
+    A = si.normal(33, 0, (M, K))
+    B = np.zeros((K, N), dtype=np.float32)
+    C0 = si.uniform_pm1(33, 2, (M, N))
+    C = run_gemm(torch, dev, A, B, C0, 1.5, -0.75, math)
+    assert np.array_equal(C, np.float32(-0.75) * C0)
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_closed_form_identity(dev, math):
+    M, N = 300, 260
+    A = np.eye(M, dtype=np.float32)
+    B = si.uniform_pm1(34, 1, (M, N))
+    C0 = si.uniform_pm1(34, 2, (M, N))
+    C, ref, _ = check(dev, A, B, C0, 0.75, 0.25, math)
+    # A = I: C = alpha*B + beta*C0
+    assert np.allclose(C, 0.75 * B.astype(np.float64) + 0.25 * C0, rtol=0,
+                       atol=4 * tolerance(math))
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_beta_zero_ignores_nan(dev, math):
+    M, N, K = 160, 140, 70
+    A = si.normal(35, 0, (M, K))
+    B = si.normal(35, 1, (K, N))
+    C0 = np.full((M, N), np.nan, dtype=np.float32)
+    C = run_gemm(torch, dev, A, B, C0, 1.0, 0.0, math)
+    assert np.isfinite(C).all()
+    ref, den = oracle.sgemm(A, B, None, 1.0, 0.0)
+    assert oracle.max_rel_error(C, ref, den) <= tolerance(math)
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_alpha_zero_and_k_zero(dev, math):
+    M, N = 100, 90
+    C0 = si.uniform_pm1(36, 2, (M, N))
+    A = si.normal(36, 0, (M, 40))
+    B = si.normal(36, 1, (40, N))
+    C = run_gemm(torch, dev, A, B, C0, 0.0, 0.5, math)
+    assert np.array_equal(C, np.float32(0.5) * C0)
+    C = run_gemm(torch, dev, np.zeros((M, 0), np.float32), np.zeros((0, N), np.float32), C0,
+                 2.0, 0.5, math)
+    assert np.array_equal(C, np.float32(0.5) * C0)
+
+
+def test_empty_output_is_untouched(dev):
+    for M, N in ((0, 10), (10, 0)):
+        st = phobos.phobos_sgemm(M, N, 5, 1.0, 16, 5, 16, max(N, 1), 0.0, 16, max(N, 1), 0)
+        assert st == phobos.PHOBOS_OK
+
+
+# --------------------------------------------------------- K-chunked super-tiles
+
+@pytest.mark.parametrize("math,super_k", [("3xtf32", 512), ("3xtf32", 96), ("tf32", 1024),
+                                          ("ffma", 520)])
+def test_k_chunked_cluster_split(dev, math, super_k):
+    M, N, K = 520, 390, 2100
+    plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, math)
+    plan.super_k = super_k
+    A = si.uniform_pm1(37, 0, (M, K))
+    B = si.uniform_pm1(37, 1, (K, N))
+    C0 = si.normal(37, 2, (M, N))
+    check(dev, A, B, C0, 0.75, 0.25, math, plan=plan)
+
+
+def test_plan_validation_on_device(dev):
+    plan = phobos.phobos_gemm_plan(256, 256, 256, 256, 256, 256, "3xtf32")
+    plan.super_k = 33  # not a multiple of the K block
+    A = torch.zeros(256, 256, device=dev)
+    with pytest.raises(phobos.PhobosError):
+        phobos.sgemm(A, A, A.clone(), 1.0, 0.0, math="3xtf32", plan=plan)
+    plan = phobos.phobos_gemm_plan(256, 256, 256, 256, 256, 256, "3xtf32")
+    with pytest.raises(phobos.PhobosError):
+        phobos.sgemm(A, A, A.clone(), 1.0, 0.0, math="ffma", plan=plan)
+
+
+def test_host_buffer_entry_point(dev):
+    M, N, K = 333, 222, 111
+    A = si.normal(38, 0, (M, K))
+    B = si.normal(38, 1, (K, N))
+    C0 = si.uniform_pm1(38, 2, (M, N))
+    C = C0.copy()
+    st = phobos.phobos_sgemm_host(M, N, K, 1.5, A.ctypes.data, K, B.ctypes.data, N, 0.5,
+                                  C.ctypes.data, N, 0, phobos.PHOBOS_MATH_3XTF32)
+    assert st == phobos.PHOBOS_OK
+    ref, den = oracle.sgemm(A, B, C0, 1.5, 0.5)
+    assert oracle.max_rel_error(C, ref, den) <= oracle.TOL_FP32
+
+
+def test_timing_events_and_launch_count(dev):
+    M = N = K = 512
+    A = torch.randn(M, K, device=dev)
+    B = torch.randn(K, N, device=dev)
+    C = torch.zeros(M, N, device=dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()  # torch creates the CUDA events lazily, on first record
+    stop.record()
+    n0 = phobos.phobos_kernel_launches()
+    phobos.phobos_set_timing_events(start.cuda_event, stop.cuda_event)
+    try:
+        phobos.sgemm(A, B, C, 1.0, 0.0, math="3xtf32")
+    finally:
+        phobos.phobos_set_timing_events(None, None)
+    torch.cuda.synchronize()
+    assert phobos.phobos_kernel_launches() - n0 == 3  # split A, split B, main kernel
+    assert start.elapsed_time(stop) > 0
