@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""SGEMM benchmark: GFLOP/s (2MNK / device time) of C = alpha*A*B + beta*C.
+
+Default workload: the 8192^3 fp32 SGEMM (A, B uniform[-1,1], C_old normal,
+alpha = 0.75, beta = 0.25, seed 2) through libphobos_gemm's default plan
+(split TF32 on the tcgen05 tensor cores).  One "step" is one full call: the
+operand pre-pass and the main kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--math M]
+  python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (the path does not shard);
+the timed region is bracketed by barriers and the max over ranks is taken.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM GFLOP/s (2MNK/device time) at 8192^3 fp32; fraction of GB300 roofline"
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25   # dense tensor rates, nominal
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+SMS, FP32_LANES_PER_SM = 152, 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["phobos", "reference"], default="phobos")
+    ap.add_argument("--workload", default="sgemm_8192")
+    ap.add_argument("--math", default="default", choices=["default", "3xtf32", "tf32", "ffma"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target host time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=150.0,
+                    help="seconds the whole --impl reference run may take")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def peak_for(path_name, peaks):
+    """Roofline denominator of the main kernel, by path."""
+    if path_name in ("3xtf32", "tf32"):
+        tf32 = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
+        return ("tensor", tf32 / 3.0 if path_name == "3xtf32" else tf32, "TFLOP/s",
+                "bf16 burst x nominal tf32/bf16 (1.1/2.25)%s" % (" / 3" if path_name == "3xtf32" else ""))
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    return ("alu", SMS * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12, "TFLOP/s",
+            "152 SMs x 128 fp32 lanes x 2 flop x max SM clock")
+
+
+def kernel_traffic(kernel_file, workload, math_name):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    or None when the kernel source changed since the counters were taken."""
+    summary = os.path.join(ROOT, "profiles", "sgemm_tc_%s_%s.md" % (math_name, workload))
+    try:
+        text = open(summary).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_sha or not m_tr:
+        return None
+    src = open(os.path.join(ROOT, "language_fp32_gemm_gb300", "csrc", kernel_file), "rb").read()
+    if hashlib.sha256(src).hexdigest() != m_sha.group(1):
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, with wall timestamps."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5.0:
+            time.sleep(0.05)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_begin, t_end):
+        rows = [s for t, s in self.samples if t_begin <= t <= t_end and len(s) >= 8]
+        if not rows:  # a short region: take the samples nearest to it
+            rows = [s for t, s in self.samples if len(s) >= 8][-3:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = sorted({name for r in rows for name, v in zip(self.REASONS, r[4:8])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def oracle_rows_rate(w, A, B, C0, seconds):
+    """Time the CPU oracle on a row sample of the workload sized to ~seconds.
+
+    Returns (GFLOP/s, rows used, threads, seconds taken)."""
+    import oracle
+    threads = oracle.default_threads()
+    rows = max(1, min(w.M, threads))
+    while True:
+        t0 = time.perf_counter()
+        oracle.sgemm(A[:rows], B, None if w.beta == 0 else C0[:rows], w.alpha, w.beta,
+                     nthreads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= seconds * 0.5 or rows >= w.M:
+            return 2.0 * rows * w.N * w.K / dt / 1e9, rows, threads, dt
+        grow = max(2.0, min(16.0, seconds * 0.8 / max(dt, 1e-3)))
+        rows = min(w.M, int(math.ceil(rows * grow)))
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import seeded_inputs as si
+    w = si.workload(args.workload)
+    A, B = w.A(), w.B()
+    C0 = w.C_old() if w.beta != 0 else None
+    threads = oracle.default_threads()
+    per_step = max(0.5, args.reference_budget / max(1, args.steps + args.warmup))
+    # calibrate rows per step on one probe
+    rows = max(1, threads)
+    t0 = time.perf_counter()
+    oracle.sgemm(A[:rows], B, None if C0 is None else C0[:rows], w.alpha, w.beta, nthreads=threads)
+    dt = time.perf_counter() - t0
+    rows = int(max(1, min(w.M, rows * per_step / max(dt, 1e-3))))
+    times = []
+    for step in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.sgemm(A[:rows], B, None if C0 is None else C0[:rows], w.alpha, w.beta,
+                     nthreads=threads)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    flops = 2.0 * rows * w.N * w.K
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e9
+    sample = "%d of %d output rows per step (%dx%dx%d), fp64 oracle, %d threads" % (
+        rows, w.M, w.M, w.N, w.K, threads)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                   "beta": w.beta, "seed": w.seed, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_phobos(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import language_fp32_gemm_gb300 as phobos
+    import seeded_inputs as si
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    phobos.library()  # fails loudly if the CUDA library is not built
+
+    w = si.workload(args.workload)
+    M, N, K = w.M, w.N, w.K
+    A_h, B_h, C_h = w.A(), w.B(), w.C_old()
+    pin = lambda x: torch.from_numpy(x).pin_memory()
+    A_p, B_p, C_p = pin(A_h), pin(B_h), pin(C_h)
+    dA, dB = A_p.to(dev), B_p.to(dev)
+    dC0 = C_p.to(dev)
+    dC = dC0.clone()
+    plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, args.math)
+    path_name = {phobos.PHOBOS_PATH_FFMA: "ffma", phobos.PHOBOS_PATH_TF32: "tf32",
+                 phobos.PHOBOS_PATH_3XTF32: "3xtf32"}[plan.path]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        phobos.sgemm(dA, dB, dC, w.alpha, w.beta, math=args.math, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = phobos.phobos_check_device(stream.cuda_stream)
+    if st != phobos.PHOBOS_OK:
+        raise SystemExit("device status after warm-up: " + phobos.status_string(st))
+
+    # per-step events around the main kernel (recorded by the library) and the step
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in kev:
+        a.record(stream)
+        b.record(stream)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = phobos.phobos_kernel_launches()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        phobos.phobos_set_timing_events(kev[i][0].cuda_event, kev[i][1].cuda_event)
+        step()
+    phobos.phobos_set_timing_events(None, None)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = phobos.phobos_kernel_launches() - launches0
+    if clocks:
+        clocks.stop()
+    st = phobos.phobos_check_device(stream.cuda_stream)
+    if st != phobos.PHOBOS_OK:
+        raise SystemExit("device status after timed region: " + phobos.status_string(st))
+
+    elapsed_ms = t_start.elapsed_time(t_stop)
+    kernel_ms = [a.elapsed_time(b) for a, b in kev]
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    flops = 2.0 * M * N * K
+    value = world * flops * args.steps / (max_ms / 1e3) / 1e9
+
+    # ------------------------------------------------ end to end, host buffers
+    C_out = torch.empty_like(C_p).pin_memory()
+    e2e_ms = []
+    for i in range(args.e2e_steps + 1):
+        C_out.copy_(C_p)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = phobos.phobos_sgemm_host(M, N, K, w.alpha, A_p.data_ptr(), K, B_p.data_ptr(), N,
+                                      w.beta, C_out.data_ptr(), N, stream.cuda_stream,
+                                      args.math)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if st != phobos.PHOBOS_OK:
+            raise SystemExit("phobos_sgemm_host: " + phobos.status_string(st))
+        if i > 0:
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = 4 * (M * K + K * N + (M * N if w.beta != 0 else 0))
+    d2h = 4 * M * N
+    e2e_t = torch.tensor([sum(e2e_ms) / len(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = world * flops / (float(e2e_t.item()) / 1e3) / 1e9
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    # ------------------------------------------------------------- roofline
+    peaks, peak_src = load_peaks()
+    bound, peak, unit, peak_note = peak_for(path_name, peaks)
+    kernel_file = "sgemm_ffma.cu" if path_name == "ffma" else "sgemm_tc.cu"
+    avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
+    achieved = flops / (avg_kernel_ms / 1e3) / 1e12
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": kernel_traffic(kernel_file, args.workload,
+                                                                    path_name),
+                "peak_source": "%s (%s)" % (peak_src, peak_note),
+                "kernel": "sgemm_tc_kernel" if path_name != "ffma" else "sgemm_ffma_kernel",
+                "kernel_ms": avg_kernel_ms,
+                "algorithmic_flops_per_launch": flops}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, rows, threads, dt = oracle_rows_rate(w, A_h, B_h, C_h, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": "%d of %d output rows of the %dx%dx%d workload (fp64 oracle), %.1f s"
+                         % (rows, M, M, N, K, dt)}
+
+    clk = clocks.summary(wall0, wall1) if clocks else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "alpha": w.alpha,
+                   "beta": w.beta, "seed": w.seed, "math": path_name,
+                   "plan": plan.as_dict(), "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (%.0f MiB of A, B, C)"
+                         % (4 * (M * K + K * N + M * N) / 2 ** 20),
+                   "step": "operand split pre-pass + main kernel, one call"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": sum(e2e_ms) / len(e2e_ms),
+                "api": "phobos_sgemm_host (pinned host buffers)"},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_phobos(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
