@@ -170,6 +170,45 @@ uint64_t phobos_kernel_launches(void);
  * Must not be called while a call of this library is running on any stream. */
 phobos_status_t phobos_release(void);
 
+/*
+ * No-allocation form of the split-TF32 (3xTF32) GEMM.  The pages have no
+ * counterpart; it exists for callers that may not allocate device memory
+ * themselves: a serving process whose device memory was reserved up front by
+ * its own allocator (a caching allocator or an engine that claimed most of
+ * HBM at start-up, where a new cudaMalloc can fail or fragment the pool), and
+ * latency-critical loops that cannot take the implicit synchronisation and
+ * latency of cudaMalloc/cudaFree.
+ *
+ * Same arguments, layout, ownership and result as phobos_sgemm_ex with
+ * PHOBOS_MATH_3XTF32 and the automatic plan.  The call allocates nothing:
+ * no cudaMalloc, cudaMallocAsync, cudaFree or other allocating routine.  Its
+ * scratch is one fixed device array inside the library
+ * (PHOBOS_NOALLOC_SCRATCH_BYTES of split operands plus a status word).  Every
+ * GPU that loads the library holds that array until the process exits.
+ *  - Limit: the split operands take 8 * (Mp + Np) * Kp bytes, where
+ *    Mp = M rounded up to 128, Np = N rounded up to 128 (N <= 128) or 256,
+ *    and Kp = K rounded up to 32.  Larger problems return
+ *    PHOBOS_ERR_UNSUPPORTED with nothing enqueued.
+ *    2048 x 2048 x 2048 fits exactly.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (with that device current).  Make that first call before any
+ *    stream capture.
+ *  - Sharing: every call, on every stream, uses the same array, and the array
+ *    keeps what the last call left there.  The operand pre-pass overwrites
+ *    every element a call reads, padding included.  Calls whose work overlaps
+ *    on the GPU (for example on two streams at once) race on the array:
+ *    serialise them.
+ *  - Errors: as phobos_sgemm_ex.  An expired device-side wait is recorded in
+ *    the array's status word.  It is reported as PHOBOS_ERR_TIMEOUT (and
+ *    cleared) only when PHOBOS_DEBUG_SYNC=1, since that check synchronises
+ *    the stream.
+ */
+#define PHOBOS_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+phobos_status_t phobos_sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const float *A, int64_t lda, const float *B,
+                                     int64_t ldb, float beta, float *C, int64_t ldc,
+                                     void *stream);
+
 /* A static, NUL-terminated description of a status code. */
 const char *phobos_status_string(phobos_status_t status);
 

@@ -42,7 +42,10 @@ MATH_NAMES = {"default": PHOBOS_MATH_DEFAULT, "3xtf32": PHOBOS_MATH_3XTF32,
 
 ABI_FUNCTIONS = ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
                  "phobos_check_device", "phobos_set_timing_events", "phobos_kernel_launches",
-                 "phobos_release", "phobos_status_string")
+                 "phobos_release", "phobos_status_string", "phobos_sgemm_noalloc")
+
+# Split operands the no-allocation entry point can hold (bytes).
+PHOBOS_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class PhobosGemmPlan(ctypes.Structure):
@@ -89,6 +92,7 @@ def library():
         lib.phobos_sgemm.argtypes = gemm
         lib.phobos_sgemm_ex.argtypes = gemm + [i32, plan_p]
         lib.phobos_sgemm_host.argtypes = gemm + [i32]
+        lib.phobos_sgemm_noalloc.argtypes = gemm
         lib.phobos_check_device.argtypes = [vp]
         lib.phobos_release.argtypes = []
         lib.phobos_set_timing_events.argtypes = [vp, vp]
@@ -97,7 +101,8 @@ def library():
         lib.phobos_status_string.argtypes = [i32]
         lib.phobos_status_string.restype = ctypes.c_char_p
         for name in ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
-                     "phobos_check_device", "phobos_release", "phobos_set_timing_events"):
+                     "phobos_check_device", "phobos_release", "phobos_set_timing_events",
+                     "phobos_sgemm_noalloc"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -137,6 +142,12 @@ def phobos_sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0,
                       math=PHOBOS_MATH_DEFAULT):
     return library().phobos_sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
                                        _math(math))
+
+
+def phobos_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0):
+    """Split-TF32 GEMM whose scratch is a fixed array inside the library: no
+    device allocation, for callers that cannot allocate (see the C header)."""
+    return library().phobos_sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def phobos_check_device(stream=0):

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libphobos_gemm.so")
-SOURCES = ["phobos_gemm.cu", "sgemm_tc.cu", "sgemm_ffma.cu", "split.cu"]
+SOURCES = ["phobos_gemm.cu", "sgemm_tc.cu", "sgemm_ffma.cu", "split.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h", os.path.join("..", "..", "include", "phobos_gemm.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
