@@ -357,13 +357,22 @@ def run_phobos(args):
     kernel_file = "sgemm_ffma.cu" if path_name == "ffma" else "sgemm_tc.cu"
     avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
     achieved = flops / (avg_kernel_ms / 1e3) / 1e12
+    clk = clocks.summary(wall0, wall1) if clocks else None
+    # Per-clock view: nominal dense tensor rate per SM (tf32: 4096 flop/clk/SM,
+    # i.e. 1.1 PFLOP/s at ~1.77 GHz) at the SM clock sampled during the run.
+    per_clock = None
+    if bound == "tensor" and clk and clk.get("sm_mhz"):
+        tf32_clk = SMS * 4096 * clk["sm_mhz"] * 1e6 / 1e12
+        per_clock = tf32_clk / 3.0 if path_name == "3xtf32" else tf32_clk
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_file, args.workload,
                                                                     path_name),
                 "peak_source": "%s (%s)" % (peak_src, peak_note),
                 "kernel": "sgemm_tc_kernel" if path_name != "ffma" else "sgemm_ffma_kernel",
                 "kernel_ms": avg_kernel_ms,
-                "algorithmic_flops_per_launch": flops}
+                "algorithmic_flops_per_launch": flops,
+                "peak_per_clock": per_clock,
+                "frac_per_clock": achieved / per_clock if per_clock else None}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -372,7 +381,6 @@ def run_phobos(args):
                "sample": "%d of %d output rows of the %dx%dx%d workload (fp64 oracle), %.1f s"
                          % (rows, M, M, N, K, dt)}
 
-    clk = clocks.summary(wall0, wall1) if clocks else None
     line = {
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,

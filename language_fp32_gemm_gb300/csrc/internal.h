@@ -50,5 +50,9 @@ struct TcArgs {
 // passes: 1 (tf32) or 3 (split tf32); bn: 128 or 256.
 cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream);
 int tc_max_stages(int passes, int bn);
+// CTA-pair (cluster of 2, tcgen05 cta_group::2) variant: tiles_m counts
+// 256-row pair tiles; bn: 256.
+cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream);
+int tc_pair_max_stages(int passes, int bn);
 
 }  // namespace phobos

@@ -148,8 +148,8 @@ phobos_status_t check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_
   return PHOBOS_OK;
 }
 
-size_t tc_workspace(int64_t M, int64_t N, int64_t K, int bn, int passes) {
-  const int64_t Mp = round_up(M, kTcBM), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
+size_t tc_workspace(int64_t M, int64_t N, int64_t K, int bm, int bn, int passes) {
+  const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
   const int64_t a = round_up(Mp * Kp * 4, 256), b = round_up(Np * Kp * 4, 256);
   return static_cast<size_t>((a + b) * (passes == 3 ? 2 : 1));
 }
@@ -187,13 +187,16 @@ phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
   } else {
     const int passes = path == PHOBOS_PATH_3XTF32 ? 3 : 1;
     const int bn = N <= 128 ? 128 : 256;
-    p->tile_m = kTcBM;
+    // A CTA pair (256-row tile, tcgen05 cta_group::2) when both extents fill it.
+    const bool pair = bn == 256 && M > kTcBM;
+    p->tile_m = pair ? 2 * kTcBM : kTcBM;
+    p->cluster_m = pair ? 2 : 1;
     p->tile_n = bn;
     p->tile_k = kTcBK;
-    p->stages = tc_max_stages(passes, bn);
+    p->stages = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
     p->super_m = kDefaultSuper;
     p->super_n = kDefaultSuper;
-    p->workspace_bytes = tc_workspace(M, N, K, bn, passes);
+    p->workspace_bytes = tc_workspace(M, N, K, p->tile_m, bn, passes);
   }
   return PHOBOS_OK;
 }
@@ -203,17 +206,22 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (math == PHOBOS_MATH_FFMA && p.path != PHOBOS_PATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
   if (math == PHOBOS_MATH_TF32 && p.path != PHOBOS_PATH_TF32) return PHOBOS_ERR_INVALID_VALUE;
   if (math == PHOBOS_MATH_3XTF32 && p.path != PHOBOS_PATH_3XTF32) return PHOBOS_ERR_INVALID_VALUE;
-  if (p.cluster_m != 1 || p.cluster_n != 1 || p.multicast != 0) return PHOBOS_ERR_UNSUPPORTED;
+  if (p.cluster_n != 1 || p.multicast != 0 || (p.cluster_m != 1 && p.cluster_m != 2))
+    return PHOBOS_ERR_UNSUPPORTED;
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
   if (p.path == PHOBOS_PATH_FFMA) {
+    if (p.cluster_m != 1) return PHOBOS_ERR_UNSUPPORTED;
     if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
       return PHOBOS_ERR_INVALID_VALUE;
     if (p.tile_k != 8 || (p.super_k < K && p.super_k % 8 != 0)) return PHOBOS_ERR_INVALID_VALUE;
   } else if (p.path == PHOBOS_PATH_TF32 || p.path == PHOBOS_PATH_3XTF32) {
     const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
-    if (p.tile_m != kTcBM || (p.tile_n != 128 && p.tile_n != 256) || p.tile_k != kTcBK)
+    const bool pair = p.cluster_m == 2;
+    if (p.tile_m != (pair ? 2 * kTcBM : kTcBM) || (p.tile_n != 128 && p.tile_n != 256) ||
+        p.tile_k != kTcBK || (pair && p.tile_n != 256))
       return PHOBOS_ERR_INVALID_VALUE;
-    if (p.stages < 2 || p.stages > tc_max_stages(passes, p.tile_n)) return PHOBOS_ERR_INVALID_VALUE;
+    const int max_st = pair ? tc_pair_max_stages(passes, p.tile_n) : tc_max_stages(passes, p.tile_n);
+    if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
     if (p.super_k < K && p.super_k % kTcBK != 0) return PHOBOS_ERR_INVALID_VALUE;
     if (round_up(N, p.tile_n) / 32 > 65535) return PHOBOS_ERR_UNSUPPORTED;
   } else {
@@ -275,9 +283,11 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
                        cudaStream_t stream, const phobos_gemm_plan_t &p, DeviceState &dev,
                        int device) {
   const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
+  const bool pair = p.cluster_m == 2;
+  const int bm = pair ? 2 * kTcBM : kTcBM;
   const int bn = p.tile_n;
-  const int64_t Mp = round_up(M, kTcBM), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
-  const size_t need = tc_workspace(M, N, K, bn, passes);
+  const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
+  const size_t need = tc_workspace(M, N, K, bm, bn, passes);
   Buffer &ws = g_workspaces[{device, reinterpret_cast<uintptr_t>(stream)}];
   phobos_status_t st = ensure_buffer(ws, need, stream);
   if (st != PHOBOS_OK) return st;
@@ -300,11 +310,13 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   if (st != PHOBOS_OK) return st;
 
   TcArgs t{};
+  // each CTA loads 128 rows of A and, in a pair, half of the tile's B rows
+  const int b_box = pair ? bn / 2 : bn;
   if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
-  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, bn)) != PHOBOS_OK) return st;
+  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, b_box)) != PHOBOS_OK) return st;
   if (passes == 3) {
     if ((st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
-    if ((st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, bn)) != PHOBOS_OK) return st;
+    if ((st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, b_box)) != PHOBOS_OK) return st;
   } else {
     t.tmap_as = t.tmap_ab;
     t.tmap_bs = t.tmap_bb;
@@ -313,9 +325,9 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   t.ldc = ldc;
   t.M = static_cast<int>(M);
   t.N = static_cast<int>(N);
-  t.tiles_m = static_cast<int>(Mp / kTcBM);
+  t.tiles_m = static_cast<int>(Mp / bm);
   t.tiles_n = static_cast<int>(Np / bn);
-  int64_t gm = p.super_m / kTcBM;
+  int64_t gm = p.super_m / bm;
   if (gm < 1) gm = 1;
   if (gm > t.tiles_m) gm = t.tiles_m;
   t.group_m = static_cast<int>(gm);
@@ -329,7 +341,8 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     t.k_block0 = 0;
     t.k_blocks = total_blocks;
     if (mark(g_ev_start, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
-    st = cuda_status(counted(launch_tc(t, passes, bn, p.stages, stream)));
+    st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream)
+                                   : launch_tc(t, passes, bn, p.stages, stream)));
     if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
     return st;
   }
@@ -342,7 +355,8 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     t.beta = 1.0f;
     t.k_block0 = kb;
     t.k_blocks = total_blocks - kb < chunk_blocks ? total_blocks - kb : chunk_blocks;
-    st = cuda_status(counted(launch_tc(t, passes, bn, p.stages, stream)));
+    st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream)
+                                   : launch_tc(t, passes, bn, p.stages, stream)));
   }
   if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
   return st;

@@ -32,6 +32,17 @@
 //  - Epilogue: fmaf(alpha, sum, beta * c_old) with 16-byte vector loads and
 //    stores where C allows and scalar edge handling.
 //
+//  - CTA pairs (PAIR = true): a thread-block cluster of two CTAs on the two
+//    SMs of one TPC computes a 256 x BN tile with tcgen05.mma.cta_group::2
+//    (the CTA-pair mode of the "Clusters et DSMEM" chapter, section 3.4: the
+//    tile grows from 128 x 128 to 256 x 128, here 256 x 256).  Each CTA TMA-loads
+//    its own 128 rows of A and its own BN/2 rows of B; the leader CTA's
+//    barrier counts both CTAs' bytes, the leader alone issues the MMAs, and
+//    each SM reads its B half once for both tensor cores, which halves the
+//    per-SM operand traffic of the single-CTA tile.  Commits are multicast to
+//    both CTAs; the peer's epilogue warps arrive on the leader's barriers
+//    through distributed shared memory.  No TMA multicast is used.
+//
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
 // MMA issuer, warps 2..9 = accumulator/epilogue warps.  Epilogue warp w reads
 // TMEM lanes 32*(w%4) .. +31 (the hardware's lane-quarter rule) and columns
@@ -43,20 +54,22 @@ namespace phobos {
 
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBK = 32;  // fp32 elements per row of one stage = 128 bytes = swizzle span
+constexpr int kBM = 128;  // A rows (and output rows) per CTA
+constexpr int kBK = 32;   // fp32 elements per row of one stage = 128 bytes = swizzle span
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemLimit = 227 * 1024;
+constexpr uint64_t kAbortGraceNs = 200000;  // let copies in flight land before exit
 
-template <int BN, int PASSES>
+template <int BN, int PASSES, bool PAIR>
 struct TcShape {
-  static constexpr int kOps = PASSES == 3 ? 2 : 1;  // big (+ small) per operand
-  static constexpr int kATile = kBM * kBK * 4;       // 16 KiB
-  static constexpr int kBTile = BN * kBK * 4;
+  static constexpr int kOps = PASSES == 3 ? 2 : 1;   // big (+ small) per operand
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows this CTA loads
+  static constexpr int kATile = kBM * kBK * 4;        // 16 KiB
+  static constexpr int kBTile = kBRows * kBK * 4;
   static constexpr int kStageBytes = kOps * (kATile + kBTile);
-  static constexpr int kTmemCols = 2 * BN;           // two accumulator buffers
-  static constexpr int kAux = 1024 + 256;            // alignment slack + barriers
+  static constexpr int kTmemCols = 2 * BN;            // two accumulator buffers
+  static constexpr int kAux = 1024 + 256;             // alignment slack + barriers
   static constexpr int max_stages() { return (kSmemLimit - kAux) / kStageBytes; }
   static constexpr int smem_bytes(int stages) { return stages * kStageBytes + kAux; }
 };
@@ -75,9 +88,9 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
   tn = r / rows;
 }
 
-template <int BN, int PASSES, int STAGES>
+template <int BN, int PASSES, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
-  using S = TcShape<BN, PASSES>;
+  using S = TcShape<BN, PASSES, PAIR>;
   constexpr int kHalf = BN / 2;  // columns summed by one epilogue thread
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -96,10 +109,18 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+
+  // Raise the abort flag of the peer CTA too, so both stop promptly.
+  auto abort_peer = [&]() {
+    if (PAIR) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u), 1u);
+  };
 
   int tm, tn;
-  raster(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-  const int m0 = tm * kBM;
+  raster(PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x), p.tiles_m,
+         p.tiles_n, p.group_m, tm, tn);
+  const int m0 = tm * (PAIR ? 2 * kBM : kBM) + static_cast<int>(rank) * kBM;
   const int n0 = tn * BN;
   const int chunk = p.promote_blocks;
   const int n_chunks = (p.k_blocks + chunk - 1) / chunk;
@@ -111,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full0 + 8u * b, 1);
-      mbar_init(acc_empty0 + 8u * b, kEpiWarps);
+      mbar_init(acc_empty0 + 8u * b, (PAIR ? 2 : 1) * kEpiWarps);
     }
     mbar_init(mma_drained, 1);
     *abort_flag = 0;
@@ -126,11 +147,20 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), S::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), S::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), S::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (PAIR)
+    cluster_sync();  // the peer's barriers are initialised before anyone signals them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -138,41 +168,70 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t armed = 0, last_parity = 0;
+      const int b_row = n0 + static_cast<int>(rank) * S::kBRows;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (kb / STAGES) & 1u;
-        if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) break;
+        if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
+          abort_peer();
+          break;
+        }
         const uint32_t full = full0 + 8u * s;
-        mbar_arrive_expect_tx(full, S::kStageBytes);
         const int kc = (p.k_block0 + kb) * kBK;
         const uint32_t st = tiles + s * S::kStageBytes;
-        tma_load_2d(st, &p.tmap_ab, full, kc, m0);
-        if (PASSES == 3) tma_load_2d(st + S::kATile, &p.tmap_as, full, kc, m0);
         const uint32_t bt = st + S::kOps * S::kATile;
-        tma_load_2d(bt, &p.tmap_bb, full, kc, n0);
-        if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, n0);
+        if (PAIR) {
+          // both CTAs' bytes complete on the leader's barrier
+          if (leader) mbar_arrive_expect_tx(full, 2 * S::kStageBytes);
+          const uint32_t lead_full = mapa_shared(full, 0);
+          tma_load_2d_pair(st, &p.tmap_ab, lead_full, kc, m0);
+          if (PASSES == 3) tma_load_2d_pair(st + S::kATile, &p.tmap_as, lead_full, kc, m0);
+          tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
+          if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
+        } else {
+          mbar_arrive_expect_tx(full, S::kStageBytes);
+          tma_load_2d(st, &p.tmap_ab, full, kc, m0);
+          if (PASSES == 3) tma_load_2d(st + S::kATile, &p.tmap_as, full, kc, m0);
+          tma_load_2d(bt, &p.tmap_bb, full, kc, b_row);
+          if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, b_row);
+        }
         armed |= 1u << s;
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
       }
-      // No bulk copy may still be writing this CTA's shared memory at exit.
-      for (int s = 0; s < STAGES; ++s)
-        if (armed & (1u << s))
-          bounded_wait(full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
-                       kDevTimeoutDrain, false);
+      // No bulk copy may still be writing shared memory at exit.  The leader's
+      // full barriers count every armed stage; a pair's peer cannot observe its
+      // own copies, so after an abort it gives them a bounded grace period.
+      if (leader) {
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s))
+            bounded_wait(full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
+                         kDevTimeoutDrain, false);
+      }
+      if (PAIR && *abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kAbortGraceNs) {
+        }
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(kBM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_tf32(PAIR ? 2 * kBM : kBM, BN);
       int kb = 0;
       bool ok = true;
       for (int c = 0; c < n_chunks && ok; ++c) {
         const int b = c & 1;
         const uint32_t use = static_cast<uint32_t>(c >> 1);
-        // the epilogue warps must have read this buffer's previous partial sum
-        if (!bounded_wait(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
-                          kDevTimeoutMma)) {
+        // the epilogue warps (of both CTAs) must have read this buffer's
+        // previous partial sum
+        const bool free_buf =
+            PAIR ? bounded_wait_cluster(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
+                                        kDevTimeoutMma)
+                 : bounded_wait(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
+                                kDevTimeoutMma);
+        if (!free_buf) {
           ok = false;
+          abort_peer();
           break;
         }
         tc_fence_after();
@@ -183,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
           const uint32_t ph = (kb / STAGES) & 1u;
           if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) {
             ok = false;
+            abort_peer();
             break;
           }
           tc_fence_after();
@@ -199,19 +259,39 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
             if (PASSES == 3) {
               const uint64_t das = desc_kmajor_sw128(a_small + off);
               const uint64_t dbs = desc_kmajor_sw128(b_small + off);
-              mma_tf32(d_tmem, das, dbb, idesc, acc);
-              mma_tf32(d_tmem, dab, dbs, idesc, 1u);
-              mma_tf32(d_tmem, dab, dbb, idesc, 1u);
+              if (PAIR) {
+                mma_tf32_pair(d_tmem, das, dbb, idesc, acc);
+                mma_tf32_pair(d_tmem, dab, dbs, idesc, 1u);
+                mma_tf32_pair(d_tmem, dab, dbb, idesc, 1u);
+              } else {
+                mma_tf32(d_tmem, das, dbb, idesc, acc);
+                mma_tf32(d_tmem, dab, dbs, idesc, 1u);
+                mma_tf32(d_tmem, dab, dbb, idesc, 1u);
+              }
             } else {
-              mma_tf32(d_tmem, dab, dbb, idesc, acc);
+              if (PAIR)
+                mma_tf32_pair(d_tmem, dab, dbb, idesc, acc);
+              else
+                mma_tf32(d_tmem, dab, dbb, idesc, acc);
             }
           }
-          mma_commit(empty0 + 8u * s);
+          if (PAIR)
+            mma_commit_pair(empty0 + 8u * s, 0x3);
+          else
+            mma_commit(empty0 + 8u * s);
         }
-        if (ok) mma_commit(acc_full0 + 8u * b);
+        if (ok) {
+          if (PAIR)
+            mma_commit_pair(acc_full0 + 8u * b, 0x3);
+          else
+            mma_commit(acc_full0 + 8u * b);
+        }
       }
       // Every MMA must be finished before TMEM is released.
-      mma_commit(mma_drained);
+      if (PAIR)
+        mma_commit_pair(mma_drained, 0x1);
+      else
+        mma_commit(mma_drained);
       bounded_wait(mma_drained, 0, abort_flag, p.err, kDevTimeoutDrain, false);
     }
   } else {
@@ -228,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
       const uint32_t use = static_cast<uint32_t>(c >> 1);
       if (!bounded_wait(acc_full0 + 8u * b, use & 1u, abort_flag, p.err, kDevTimeoutEpilogue)) {
         ok = false;
+        abort_peer();
         break;
       }
       tc_fence_after();
@@ -242,7 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty0 + 8u * b);
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(mapa_shared(acc_empty0 + 8u * b, 0));
+        else
+          mbar_arrive(acc_empty0 + 8u * b);
+      }
     }
     if (ok) {
       const int row = m0 + q * 32 + lane;
@@ -281,51 +367,83 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (PAIR)
+    cluster_sync();  // the leader's MMAs read the peer's shared memory until here
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, S::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, S::kTmemCols);
   }
 }
 
-template <int BN, int PASSES, int STAGES>
+template <int BN, int PASSES, int STAGES, bool PAIR>
 cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
-  using S = TcShape<BN, PASSES>;
+  using S = TcShape<BN, PASSES, PAIR>;
   static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
-  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES>;
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR>;
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(a.tiles_m) * static_cast<unsigned>(a.tiles_n);
-  kern<<<grid, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  const unsigned tiles = static_cast<unsigned>(a.tiles_m) * static_cast<unsigned>(a.tiles_n);
+  if (!PAIR) {
+    kern<<<tiles, kThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * tiles, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int BN, int PASSES>
+template <int BN, int PASSES, bool PAIR>
 cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream) {
-  constexpr int kMax = TcShape<BN, PASSES>::max_stages();
-  if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2)>(a, stream);
-  if (stages >= 3 && kMax >= 3) return launch_one<BN, PASSES, (kMax >= 3 ? 3 : 2)>(a, stream);
-  if (stages >= 2) return launch_one<BN, PASSES, 2>(a, stream);
+  constexpr int kMax = TcShape<BN, PASSES, PAIR>::max_stages();
+  if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2), PAIR>(a, stream);
+  if (stages >= 3 && kMax >= 3) return launch_one<BN, PASSES, (kMax >= 3 ? 3 : 2), PAIR>(a, stream);
+  if (stages >= 2) return launch_one<BN, PASSES, 2, PAIR>(a, stream);
   return cudaErrorInvalidValue;
+}
+
+template <bool PAIR>
+int max_stages_of(int passes, int bn) {
+  int m = 0;
+  if (passes == 3 && bn == 256) m = TcShape<256, 3, PAIR>::max_stages();
+  if (passes == 3 && bn == 128) m = TcShape<128, 3, PAIR>::max_stages();
+  if (passes == 1 && bn == 256) m = TcShape<256, 1, PAIR>::max_stages();
+  if (passes == 1 && bn == 128) m = TcShape<128, 1, PAIR>::max_stages();
+  return m > 4 ? 4 : m;
 }
 
 }  // namespace
 
-int tc_max_stages(int passes, int bn) {
-  int m = 0;
-  if (passes == 3 && bn == 256) m = TcShape<256, 3>::max_stages();
-  if (passes == 3 && bn == 128) m = TcShape<128, 3>::max_stages();
-  if (passes == 1 && bn == 256) m = TcShape<256, 1>::max_stages();
-  if (passes == 1 && bn == 128) m = TcShape<128, 1>::max_stages();
-  return m > 4 ? 4 : m;
-}
+int tc_max_stages(int passes, int bn) { return max_stages_of<false>(passes, bn); }
+int tc_pair_max_stages(int passes, int bn) { return max_stages_of<true>(passes, bn); }
 
 cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream) {
-  if (passes == 3 && bn == 256) return launch_stages<256, 3>(a, stages, stream);
-  if (passes == 3 && bn == 128) return launch_stages<128, 3>(a, stages, stream);
-  if (passes == 1 && bn == 256) return launch_stages<256, 1>(a, stages, stream);
-  if (passes == 1 && bn == 128) return launch_stages<128, 1>(a, stages, stream);
+  if (passes == 3 && bn == 256) return launch_stages<256, 3, false>(a, stages, stream);
+  if (passes == 3 && bn == 128) return launch_stages<128, 3, false>(a, stages, stream);
+  if (passes == 1 && bn == 256) return launch_stages<256, 1, false>(a, stages, stream);
+  if (passes == 1 && bn == 128) return launch_stages<128, 1, false>(a, stages, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream) {
+  if (passes == 3 && bn == 256) return launch_stages<256, 3, true>(a, stages, stream);
+  if (passes == 1 && bn == 256) return launch_stages<256, 1, true>(a, stages, stream);
   return cudaErrorInvalidValue;
 }
 

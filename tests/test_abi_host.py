@@ -78,19 +78,22 @@ def test_plan_paths(lib):
     assert p.path == phobos.PHOBOS_PATH_FFMA and p.workspace_bytes == 0
     p = phobos.phobos_gemm_plan(8192, 8192, 8192, 8192, 8192, 8192)
     assert p.path == phobos.PHOBOS_PATH_3XTF32
-    assert p.tile_m == 128 and p.tile_n == 256 and p.tile_k == 32 and p.stages >= 2
+    assert p.tile_m == 256 and p.cluster_m == 2 and p.tile_n == 256 and p.tile_k == 32
+    assert p.stages >= 2
     assert p.super_k == 8192 and p.super_m == 4096
     # split operands: (Mp + Np) * Kp * 4 bytes, big and small
     assert p.workspace_bytes == 2 * (8192 + 8192) * 8192 * 4
     p = phobos.phobos_gemm_plan(8192, 8192, 8192, 8192, 8192, 8192, "tf32")
     assert p.path == phobos.PHOBOS_PATH_TF32 and p.workspace_bytes == (8192 + 8192) * 8192 * 4
     p = phobos.phobos_gemm_plan(3001, 5003, 1999, 1999, 5003, 5003)
-    Mp, Np, Kp = 3072, 5120, 2016
+    Mp, Np, Kp = 3072, 5120, 2016  # 256-row pair tiles, 256-column tiles, K blocks of 32
     assert p.workspace_bytes == 2 * (Mp * Kp * 4 + Np * Kp * 4)
     p = phobos.phobos_gemm_plan(65536, 256, 4096, 4096, 256, 256)
     assert p.tile_n == 256
     p = phobos.phobos_gemm_plan(4096, 100, 4096, 4096, 100, 100)
-    assert p.tile_n == 128
+    assert p.tile_n == 128 and p.tile_m == 128 and p.cluster_m == 1
+    p = phobos.phobos_gemm_plan(128, 4096, 4096, 4096, 4096, 4096)
+    assert p.tile_m == 128 and p.cluster_m == 1
     p = phobos.phobos_gemm_plan(8, 4096, 4096, 4096, 4096, 4096)
     assert p.path == phobos.PHOBOS_PATH_FFMA
 
