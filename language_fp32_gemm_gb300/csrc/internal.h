@@ -45,6 +45,7 @@ struct TcArgs {
   float alpha, beta;
   int vec_c;
   int promote_blocks;  // K blocks per TMEM partial sum before it is added into registers
+  int sm_count;        // SMs of the device: the persistent grid size
   int *err;
 };
 // passes: 1 (tf32) or 3 (split tf32); bn: 128 or 256.

@@ -37,12 +37,13 @@ constexpr int kMaxDevices = 64;
 // The scratch.  Every GPU that loads this library holds it until the process
 // exits.  Layout: [0, 4) device status word; [256, 256 + kScratchBytes) the
 // split operands of the current call.
-__device__ __align__(256) unsigned char g_noalloc_scratch[kHeadBytes + kScratchBytes];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kHeadBytes + kScratchBytes];
 
 std::mutex g_setup_mutex;
 // Device address of g_noalloc_scratch per device ordinal (0 = not set up yet).
 void *g_scratch_addr[kMaxDevices] = {};
 bool g_device_ok[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_fn = nullptr;
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -62,6 +63,9 @@ phobos_status_t set_up(int dev, void **scratch) {
       return PHOBOS_ERR_CUDA;
     g_device_ok[dev] = (major == 10 && minor == 3);
     if (!g_device_ok[dev]) return PHOBOS_ERR_UNSUPPORTED;
+    if (cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
+      return PHOBOS_ERR_CUDA;
     void *addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) {
       cudaGetLastError();
@@ -174,6 +178,7 @@ extern "C" phobos_status_t phobos_sgemm_noalloc(int64_t M, int64_t N, int64_t K,
       t.beta = beta;
       t.vec_c = (ldc % 4 == 0) && aligned16(C);
       t.promote_blocks = kPromote;
+      t.sm_count = g_sm_count[dev];
       t.err = status_word;
       st = ok(launch_tc(t, 3, bn, tc_max_stages(3, bn), stream));
     }

@@ -36,6 +36,7 @@ std::mutex g_host_mutex;  // serialises the host-buffer entry point (shared stag
 struct DeviceState {
   bool checked = false;
   bool supported = false;
+  int sm_count = 0;
   int *err = nullptr;  // device status word
 };
 std::map<int, DeviceState> g_devices;
@@ -83,6 +84,8 @@ phobos_status_t device_state(DeviceState **out, int *dev_out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return PHOBOS_ERR_CUDA;
     st.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
     st.checked = true;
   }
   if (!st.supported) return PHOBOS_ERR_UNSUPPORTED;
@@ -332,7 +335,10 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   if (gm > t.tiles_m) gm = t.tiles_m;
   t.group_m = static_cast<int>(gm);
   t.vec_c = (ldc % 4 == 0) && aligned16(C);
-  t.promote_blocks = kPromoteBlocks;
+  // Split TF32 needs short TMEM partial sums to stay at fp32 accuracy; single
+  // TF32 (a 2^-10 bound) promotes every K = 1024 only.
+  t.promote_blocks = passes == 3 ? kPromoteBlocks : 4 * kPromoteBlocks;
+  t.sm_count = dev.sm_count;
   t.err = dev.err;
   const int total_blocks = static_cast<int>(Kp / kTcBK);
   if (p.super_k >= K) {

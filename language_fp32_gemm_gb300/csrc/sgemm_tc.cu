@@ -43,6 +43,11 @@
 //    both CTAs; the peer's epilogue warps arrive on the leader's barriers
 //    through distributed shared memory.  No TMA multicast is used.
 //
+// The kernel is persistent: one CTA (or CTA pair) per SM (pair) loops over the
+// output tiles with a static stride.  Ring slots, phases and TMEM buffers run
+// on across tiles, so the next tile's loads and MMAs start while the epilogue
+// warps still store the previous tile from registers.
+//
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
 // MMA issuer, warps 2..9 = accumulator/epilogue warps.  Epilogue warp w reads
 // TMEM lanes 32*(w%4) .. +31 (the hardware's lane-quarter rule) and columns
@@ -117,11 +122,12 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     if (PAIR) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u), 1u);
   };
 
-  int tm, tn;
-  raster(PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x), p.tiles_m,
-         p.tiles_n, p.group_m, tm, tn);
-  const int m0 = tm * (PAIR ? 2 * kBM : kBM) + static_cast<int>(rank) * kBM;
-  const int n0 = tn * BN;
+  // Persistent: each CTA (pair) walks the output tiles unit, unit + units, ...
+  // in raster order, so the tiles in flight at one time are neighbours.
+  constexpr int kTileM = PAIR ? 2 * kBM : kBM;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int total_tiles = p.tiles_m * p.tiles_n;
   const int chunk = p.promote_blocks;
   const int n_chunks = (p.k_blocks + chunk - 1) / chunk;
 
@@ -168,35 +174,43 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t armed = 0, last_parity = 0;
-      const int b_row = n0 + static_cast<int>(rank) * S::kBRows;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1u;
-        if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
-          abort_peer();
-          break;
+      int g = 0;  // k blocks loaded so far by this CTA: ring slot and phase
+      bool ok = true;
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        int tm, tn;
+        raster(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        const int m0 = tm * kTileM + static_cast<int>(rank) * kBM;
+        const int b_row = tn * BN + static_cast<int>(rank) * S::kBRows;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1u;
+          if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
+            abort_peer();
+            ok = false;
+            break;
+          }
+          const uint32_t full = full0 + 8u * s;
+          const int kc = (p.k_block0 + kb) * kBK;
+          const uint32_t st = tiles + s * S::kStageBytes;
+          const uint32_t bt = st + S::kOps * S::kATile;
+          if (PAIR) {
+            // both CTAs' bytes complete on the leader's barrier
+            if (leader) mbar_arrive_expect_tx(full, 2 * S::kStageBytes);
+            const uint32_t lead_full = mapa_shared(full, 0);
+            tma_load_2d_pair(st, &p.tmap_ab, lead_full, kc, m0);
+            if (PASSES == 3) tma_load_2d_pair(st + S::kATile, &p.tmap_as, lead_full, kc, m0);
+            tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
+            if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
+          } else {
+            mbar_arrive_expect_tx(full, S::kStageBytes);
+            tma_load_2d(st, &p.tmap_ab, full, kc, m0);
+            if (PASSES == 3) tma_load_2d(st + S::kATile, &p.tmap_as, full, kc, m0);
+            tma_load_2d(bt, &p.tmap_bb, full, kc, b_row);
+            if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, b_row);
+          }
+          armed |= 1u << s;
+          last_parity = (last_parity & ~(1u << s)) | (ph << s);
         }
-        const uint32_t full = full0 + 8u * s;
-        const int kc = (p.k_block0 + kb) * kBK;
-        const uint32_t st = tiles + s * S::kStageBytes;
-        const uint32_t bt = st + S::kOps * S::kATile;
-        if (PAIR) {
-          // both CTAs' bytes complete on the leader's barrier
-          if (leader) mbar_arrive_expect_tx(full, 2 * S::kStageBytes);
-          const uint32_t lead_full = mapa_shared(full, 0);
-          tma_load_2d_pair(st, &p.tmap_ab, lead_full, kc, m0);
-          if (PASSES == 3) tma_load_2d_pair(st + S::kATile, &p.tmap_as, lead_full, kc, m0);
-          tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
-          if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
-        } else {
-          mbar_arrive_expect_tx(full, S::kStageBytes);
-          tma_load_2d(st, &p.tmap_ab, full, kc, m0);
-          if (PASSES == 3) tma_load_2d(st + S::kATile, &p.tmap_as, full, kc, m0);
-          tma_load_2d(bt, &p.tmap_bb, full, kc, b_row);
-          if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, b_row);
-        }
-        armed |= 1u << s;
-        last_parity = (last_parity & ~(1u << s)) | (ph << s);
       }
       // No bulk copy may still be writing shared memory at exit.  The leader's
       // full barriers count every armed stage; a pair's peer cannot observe its
@@ -216,75 +230,79 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_tf32(PAIR ? 2 * kBM : kBM, BN);
-      int kb = 0;
+      constexpr uint32_t idesc = idesc_tf32(kTileM, BN);
+      int g = 0;       // k blocks consumed: ring slot and phase
+      int c_glob = 0;  // partial sums produced: TMEM buffer and its phase
       bool ok = true;
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        const int b = c & 1;
-        const uint32_t use = static_cast<uint32_t>(c >> 1);
-        // the epilogue warps (of both CTAs) must have read this buffer's
-        // previous partial sum
-        const bool free_buf =
-            PAIR ? bounded_wait_cluster(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
-                                        kDevTimeoutMma)
-                 : bounded_wait(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
-                                kDevTimeoutMma);
-        if (!free_buf) {
-          ok = false;
-          abort_peer();
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-        const int kb_end = min(p.k_blocks, kb + chunk);
-        for (int first = 1; kb < kb_end; ++kb, first = 0) {
-          const int s = kb % STAGES;
-          const uint32_t ph = (kb / STAGES) & 1u;
-          if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) {
+      for (int t = unit; t < total_tiles && ok; t += units) {
+        int kb = 0;
+        for (int c = 0; c < n_chunks && ok; ++c, ++c_glob) {
+          const int b = c_glob & 1;
+          const uint32_t use = static_cast<uint32_t>(c_glob >> 1);
+          // the epilogue warps (of both CTAs) must have read this buffer's
+          // previous partial sum
+          const bool free_buf =
+              PAIR ? bounded_wait_cluster(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag,
+                                          p.err, kDevTimeoutMma)
+                   : bounded_wait(acc_empty0 + 8u * b, (use & 1u) ^ 1u, abort_flag, p.err,
+                                  kDevTimeoutMma);
+          if (!free_buf) {
             ok = false;
             abort_peer();
             break;
           }
           tc_fence_after();
-          const uint32_t a_big = tiles + s * S::kStageBytes;
-          const uint32_t a_small = a_big + S::kATile;
-          const uint32_t b_big = a_big + S::kOps * S::kATile;
-          const uint32_t b_small = b_big + S::kBTile;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 8; ++kk) {
-            const uint32_t off = kk * 32u;  // 8 tf32 = 32 bytes along K
-            const uint64_t dab = desc_kmajor_sw128(a_big + off);
-            const uint64_t dbb = desc_kmajor_sw128(b_big + off);
-            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-            if (PASSES == 3) {
-              const uint64_t das = desc_kmajor_sw128(a_small + off);
-              const uint64_t dbs = desc_kmajor_sw128(b_small + off);
-              if (PAIR) {
-                mma_tf32_pair(d_tmem, das, dbb, idesc, acc);
-                mma_tf32_pair(d_tmem, dab, dbs, idesc, 1u);
-                mma_tf32_pair(d_tmem, dab, dbb, idesc, 1u);
-              } else {
-                mma_tf32(d_tmem, das, dbb, idesc, acc);
-                mma_tf32(d_tmem, dab, dbs, idesc, 1u);
-                mma_tf32(d_tmem, dab, dbb, idesc, 1u);
-              }
-            } else {
-              if (PAIR)
-                mma_tf32_pair(d_tmem, dab, dbb, idesc, acc);
-              else
-                mma_tf32(d_tmem, dab, dbb, idesc, acc);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+          const int kb_end = min(p.k_blocks, kb + chunk);
+          for (int first = 1; kb < kb_end; ++kb, ++g, first = 0) {
+            const int s = g % STAGES;
+            const uint32_t ph = (g / STAGES) & 1u;
+            if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) {
+              ok = false;
+              abort_peer();
+              break;
             }
+            tc_fence_after();
+            const uint32_t a_big = tiles + s * S::kStageBytes;
+            const uint32_t a_small = a_big + S::kATile;
+            const uint32_t b_big = a_big + S::kOps * S::kATile;
+            const uint32_t b_small = b_big + S::kBTile;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 8; ++kk) {
+              const uint32_t off = kk * 32u;  // 8 tf32 = 32 bytes along K
+              const uint64_t dab = desc_kmajor_sw128(a_big + off);
+              const uint64_t dbb = desc_kmajor_sw128(b_big + off);
+              const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+              if (PASSES == 3) {
+                const uint64_t das = desc_kmajor_sw128(a_small + off);
+                const uint64_t dbs = desc_kmajor_sw128(b_small + off);
+                if (PAIR) {
+                  mma_tf32_pair(d_tmem, das, dbb, idesc, acc);
+                  mma_tf32_pair(d_tmem, dab, dbs, idesc, 1u);
+                  mma_tf32_pair(d_tmem, dab, dbb, idesc, 1u);
+                } else {
+                  mma_tf32(d_tmem, das, dbb, idesc, acc);
+                  mma_tf32(d_tmem, dab, dbs, idesc, 1u);
+                  mma_tf32(d_tmem, dab, dbb, idesc, 1u);
+                }
+              } else {
+                if (PAIR)
+                  mma_tf32_pair(d_tmem, dab, dbb, idesc, acc);
+                else
+                  mma_tf32(d_tmem, dab, dbb, idesc, acc);
+              }
+            }
+            if (PAIR)
+              mma_commit_pair(empty0 + 8u * s, 0x3);
+            else
+              mma_commit(empty0 + 8u * s);
           }
-          if (PAIR)
-            mma_commit_pair(empty0 + 8u * s, 0x3);
-          else
-            mma_commit(empty0 + 8u * s);
-        }
-        if (ok) {
-          if (PAIR)
-            mma_commit_pair(acc_full0 + 8u * b, 0x3);
-          else
-            mma_commit(acc_full0 + 8u * b);
+          if (ok) {
+            if (PAIR)
+              mma_commit_pair(acc_full0 + 8u * b, 0x3);
+            else
+              mma_commit(acc_full0 + 8u * b);
+          }
         }
       }
       // Every MMA must be finished before TMEM is released.
@@ -299,40 +317,46 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     const int q = warp & 3;              // TMEM lane quarter this warp may read
     const int h = (warp - 2) >> 2;       // column half
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float sum[kHalf];
-#pragma unroll
-    for (int j = 0; j < kHalf; ++j) sum[j] = 0.f;
+    int c_glob = 0;
     bool ok = true;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int b = c & 1;
-      const uint32_t use = static_cast<uint32_t>(c >> 1);
-      if (!bounded_wait(acc_full0 + 8u * b, use & 1u, abort_flag, p.err, kDevTimeoutEpilogue)) {
-        ok = false;
-        abort_peer();
-        break;
-      }
-      tc_fence_after();
-      const uint32_t col = tmem_base + static_cast<uint32_t>(b * BN + h * kHalf);
+    for (int t = unit; t < total_tiles && ok; t += units) {
+      int tm, tn;
+      raster(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      float sum[kHalf];
 #pragma unroll
-      for (int j = 0; j < kHalf; j += 32) {
-        uint32_t r[32];
-        tmem_ld32(col + lane_base + j, r);
-        tmem_ld_wait(r);
+      for (int j = 0; j < kHalf; ++j) sum[j] = 0.f;
+      for (int c = 0; c < n_chunks; ++c, ++c_glob) {
+        const int b = c_glob & 1;
+        const uint32_t use = static_cast<uint32_t>(c_glob >> 1);
+        if (!bounded_wait(acc_full0 + 8u * b, use & 1u, abort_flag, p.err, kDevTimeoutEpilogue)) {
+          ok = false;
+          abort_peer();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col = tmem_base + static_cast<uint32_t>(b * BN + h * kHalf);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) sum[j + t] = __fadd_rn(sum[j + t], __uint_as_float(r[t]));
+        for (int j = 0; j < kHalf; j += 32) {
+          uint32_t r[32];
+          tmem_ld32(col + lane_base + j, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) sum[j + u] = __fadd_rn(sum[j + u], __uint_as_float(r[u]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(mapa_shared(acc_empty0 + 8u * b, 0));
+          else
+            mbar_arrive(acc_empty0 + 8u * b);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR)
-          mbar_arrive_cluster(mapa_shared(acc_empty0 + 8u * b, 0));
-        else
-          mbar_arrive(acc_empty0 + 8u * b);
-      }
-    }
-    if (ok) {
-      const int row = m0 + q * 32 + lane;
-      const int col0 = n0 + h * kHalf;
+      if (!ok) break;
+      // The tile's sum is in registers: TMEM already serves the next tile's
+      // MMAs while this store runs.
+      const int row = tm * kTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
+      const int col0 = tn * BN + h * kHalf;
       if (row < p.M && col0 < p.N) {
         float *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
         const float alpha = p.alpha, beta = p.beta;
@@ -389,13 +413,17 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned tiles = static_cast<unsigned>(a.tiles_m) * static_cast<unsigned>(a.tiles_n);
+  const long long tiles = static_cast<long long>(a.tiles_m) * a.tiles_n;
+  // one CTA (pair) per SM (pair), never more than there are tiles
+  const long long workers = PAIR ? a.sm_count / 2 : a.sm_count;
+  const unsigned units = static_cast<unsigned>(tiles < workers ? tiles : workers);
+  if (units == 0) return cudaErrorInvalidValue;
   if (!PAIR) {
-    kern<<<tiles, kThreads, smem, stream>>>(a);
+    kern<<<units, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * tiles, 1, 1);
+  cfg.gridDim = dim3(2 * units, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
