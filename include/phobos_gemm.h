@@ -31,7 +31,10 @@
  *    PHOBOS_OK, except that PHOBOS_ERR_CUDA may follow a partial enqueue.
  *    Device-side bounded waits that expire set a device status word; it is
  *    read (and cleared) by phobos_check_device, and by every call when the
- *    environment variable PHOBOS_DEBUG_SYNC=1 is set.
+ *    environment variable PHOBOS_DEBUG_SYNC=1 is set.  For testing that path,
+ *    PHOBOS_TEST_WITHHOLD_LOAD=1 makes the tensor-core kernel skip its first
+ *    operand load: its wait on that load expires after about two seconds, the
+ *    kernel stops without writing C, and the status word reports it.
  *  - Thread safety: calls may come from several host threads.  Calls that
  *    share one stream are ordered by it; calls on different streams use
  *    different workspaces.

@@ -46,6 +46,7 @@ struct TcArgs {
   int vec_c;
   int promote_blocks;  // K blocks per TMEM partial sum before it is added into registers
   int sm_count;        // SMs of the device: the persistent grid size
+  int withhold_first_load;  // testing only: skip the first operand load (a wait then expires)
   int *err;
 };
 // passes: 1 (tf32) or 3 (split tf32); bn: 128 or 256.

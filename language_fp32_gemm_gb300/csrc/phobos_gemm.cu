@@ -339,6 +339,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   // TF32 (a 2^-10 bound) promotes every K = 1024 only.
   t.promote_blocks = passes == 3 ? kPromoteBlocks : 4 * kPromoteBlocks;
   t.sm_count = dev.sm_count;
+  t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD") ? 1 : 0;
   t.err = dev.err;
   const int total_blocks = static_cast<int>(Kp / kTcBK);
   if (p.super_k >= K) {

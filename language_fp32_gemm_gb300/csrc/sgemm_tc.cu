@@ -184,6 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
         for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1u;
+          // Failure-detection test: the first stage is never loaded, so the
+          // MMA issuer's bounded wait on it expires and the kernel aborts.
+          if (p.withhold_first_load && g == 0) continue;
           if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
             abort_peer();
             ok = false;

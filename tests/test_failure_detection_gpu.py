@@ -1,0 +1,67 @@
+"""Failure detection on the GPU without a GPU fault.
+
+Every mbarrier wait in the tensor-core kernel is bounded (about two seconds);
+when one expires the kernel records where in a device status word, stops all
+of its roles (both CTAs of a pair), releases its tensor memory and returns.
+PHOBOS_TEST_WITHHOLD_LOAD=1 makes the producer skip the first operand load, so
+the MMA issuer's wait for it runs out.  The test checks that the host reads
+PHOBOS_ERR_TIMEOUT and that the context stays usable: the next call is
+correct.  Nothing here faults, traps or hangs the GPU.
+"""
+import numpy as np
+import pytest
+
+import language_fp32_gemm_gb300 as phobos
+import oracle
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from language_fp32_gemm_gb300 import build as lib_build
+    lib_build.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.mark.parametrize("shape", [(128, 256, 96), (256, 256, 96)], ids=["single_cta", "cta_pair"])
+def test_expired_wait_is_reported_and_context_survives(dev, shape, monkeypatch):
+    M, N, K = shape
+    plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
+    assert plan.cluster_m == (2 if M > 128 else 1)
+    A = si.normal(71, 0, (M, K))
+    B = si.normal(71, 1, (K, N))
+    dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    dC = torch.full((M, N), 5.0, device=dev)
+    assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK  # nothing pending
+    monkeypatch.setenv("PHOBOS_TEST_WITHHOLD_LOAD", "1")
+    phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32")
+    st = phobos.phobos_check_device(0)
+    monkeypatch.delenv("PHOBOS_TEST_WITHHOLD_LOAD")
+    assert st == phobos.PHOBOS_ERR_TIMEOUT, phobos.status_string(st)
+    assert bool((dC == 5.0).all())  # the aborted kernel wrote nothing
+    assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK  # the word was cleared
+    # the context is intact: a normal call gives the right answer
+    phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32")
+    assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK
+    ref, den = oracle.sgemm(A, B, None, 1.0, 0.0)
+    assert oracle.max_rel_error(dC.cpu().numpy(), ref, den) <= oracle.TOL_FP32
+
+
+def test_workspace_allocation_failure_is_reported(dev):
+    # A workspace of about a terabyte cannot be allocated; the call must say so
+    # before launching anything (no operand is read).
+    M = N = 1 << 20
+    K = 1 << 16
+    x = torch.zeros(16, device=dev)
+    st = phobos.phobos_sgemm_ex(M, N, K, 1.0, x.data_ptr(), K, x.data_ptr(), N, 0.0,
+                                x.data_ptr(), N, 0, phobos.PHOBOS_MATH_3XTF32)
+    assert st == phobos.PHOBOS_ERR_OUT_OF_MEMORY
+    torch.cuda.synchronize()
+    assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK
