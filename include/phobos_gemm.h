@@ -86,7 +86,14 @@ typedef enum {
  *  super_k         K chunk of the cluster split: super_k < K runs an init
  *                  leaf C = beta*C then one step leaf C += alpha*A_c*B_c per
  *                  chunk (results equal up to rounding order).
- *  workspace_bytes device workspace the call needs.
+ *  workspace_bytes device workspace of the operand pre-pass (the tail split
+ *                  below adds at most one tile of partial sums per CTA pair,
+ *                  about 20 MB on GB300, plus flags).
+ *  tail_split      tensor-core paths: K pieces for each tile of the last,
+ *                  partial wave of the persistent grid, so idle SMs share the
+ *                  tail (0 = chosen from the SM count, 1 = off, 2..8 = that
+ *                  many, capped so every piece spans at least K = 128).
+ *                  Results are equal up to rounding order and deterministic.
  */
 typedef struct {
   int32_t path;
@@ -96,6 +103,7 @@ typedef struct {
   int32_t multicast;
   int64_t super_m, super_n, super_k;
   size_t workspace_bytes;
+  int32_t tail_split;
 } phobos_gemm_plan_t;
 
 /*

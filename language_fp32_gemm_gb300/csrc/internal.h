@@ -47,6 +47,17 @@ struct TcArgs {
   int promote_blocks;  // K blocks per TMEM partial sum before it is added into registers
   int sm_count;        // SMs of the device: the persistent grid size
   int withhold_first_load;  // testing only: skip the first operand load (a wait then expires)
+  // Split of the last, partial wave along K (0 or 1 = off).  Tiles
+  // [0, full_tiles) are computed whole; each of the remaining tiles is cut
+  // into tail_split K pieces.  Piece p > 0 writes its sum to partials slot
+  // (tile - full_tiles) * (tail_split - 1) + p - 1 (tile_m x BN floats), and
+  // each accumulator warp stores `epoch` into flags[(slot * 2 + cta rank) * 8
+  // + warp - 2]; piece 0 adds the slots in order and stores C.
+  int full_tiles, tail_split;
+  int grid_units;  // CTAs (pairs) to launch; 0 = min(tiles, SMs (pairs))
+  float *partials;
+  unsigned *flags;
+  unsigned epoch;
   int *err;
 };
 // passes: 1 (tf32) or 3 (split tf32); bn: 128 or 256.

@@ -29,6 +29,10 @@ constexpr int64_t kDefaultSuper = 4096;                 // super-tile edge (rast
 // K blocks (of 32) summed in TMEM before the partial sum is added into fp32
 // registers with round-to-nearest adds: 8 blocks = K of 256.
 constexpr int kPromoteBlocks = 8;
+// Tail split: at most this many K pieces per tile, each at least this many K blocks.
+constexpr int kMaxTailSplit = 8;
+constexpr int kMinPieceBlocks = 4;
+constexpr int kEpiWarps = 8;  // accumulator warps of the tensor-core kernel (one flag each)
 
 std::mutex g_mutex;       // planner caches, device state, workspaces
 std::mutex g_host_mutex;  // serialises the host-buffer entry point (shared staging)
@@ -212,6 +216,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (p.cluster_n != 1 || p.multicast != 0 || (p.cluster_m != 1 && p.cluster_m != 2))
     return PHOBOS_ERR_UNSUPPORTED;
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
+  if (p.tail_split < 0 || p.tail_split > kMaxTailSplit) return PHOBOS_ERR_INVALID_VALUE;
   if (p.path == PHOBOS_PATH_FFMA) {
     if (p.cluster_m != 1) return PHOBOS_ERR_UNSUPPORTED;
     if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
@@ -290,10 +295,39 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int bm = pair ? 2 * kTcBM : kTcBM;
   const int bn = p.tile_n;
   const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
-  const size_t need = tc_workspace(M, N, K, bm, bn, passes);
+  const size_t ops_bytes = tc_workspace(M, N, K, bm, bn, passes);
+
+  // Persistent grid: one CTA (pair) per SM (pair).  Split the tiles of the
+  // last, partial wave along K so that idle SMs share the tail.
+  const int units = pair ? dev.sm_count / 2 : dev.sm_count;
+  const int total_tiles = static_cast<int>((Mp / bm) * (Np / bn));
+  const int chunk_blocks_max =
+      static_cast<int>(round_up(p.super_k < K ? p.super_k : K, kTcBK) / kTcBK);
+  int tail_split = 1, full_tiles = total_tiles;
+  const int tail = units > 0 ? total_tiles % units : 0;
+  if (p.tail_split != 1 && tail != 0) {
+    int S = p.tail_split >= 2 ? p.tail_split : units / tail;
+    if (S > kMaxTailSplit) S = kMaxTailSplit;
+    if (S > chunk_blocks_max / kMinPieceBlocks) S = chunk_blocks_max / kMinPieceBlocks;
+    if (S * tail > units) S = units / tail;
+    if (S >= 2) {
+      tail_split = S;
+      full_tiles = total_tiles - tail;
+    }
+  }
+  const int64_t slots = tail_split > 1 ? static_cast<int64_t>(tail) * (tail_split - 1) : 0;
+  const size_t part_bytes = static_cast<size_t>(round_up(slots * bm * bn * 4, 256));
+  const size_t flag_bytes = static_cast<size_t>(round_up(slots * 2 * kEpiWarps * 4, 256));
+  const size_t need = ops_bytes + part_bytes + flag_bytes;
   Buffer &ws = g_workspaces[{device, reinterpret_cast<uintptr_t>(stream)}];
   phobos_status_t st = ensure_buffer(ws, need, stream);
   if (st != PHOBOS_OK) return st;
+  float *partials = reinterpret_cast<float *>(static_cast<char *>(ws.ptr) + ops_bytes);
+  unsigned *flags =
+      reinterpret_cast<unsigned *>(static_cast<char *>(ws.ptr) + ops_bytes + part_bytes);
+  // Flags must not hold a value a launch of this call will wait for.
+  if (flag_bytes && cudaMemsetAsync(flags, 0, flag_bytes, stream) != cudaSuccess)
+    return PHOBOS_ERR_CUDA;
   if ((st = get_encoder()) != PHOBOS_OK) return st;
 
   char *base = static_cast<char *>(ws.ptr);
@@ -340,6 +374,15 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   t.promote_blocks = passes == 3 ? kPromoteBlocks : 4 * kPromoteBlocks;
   t.sm_count = dev.sm_count;
   t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD") ? 1 : 0;
+  t.full_tiles = full_tiles;
+  t.tail_split = tail_split;
+  // every K piece of the tail needs its own CTA (pair); whole tiles stride over
+  // all SMs (pairs)
+  t.grid_units = tail_split > 1 ? (full_tiles > 0 ? units : tail * tail_split)
+                                : (total_tiles < units ? total_tiles : units);
+  t.partials = partials;
+  t.flags = flags;
+  t.epoch = 1;
   t.err = dev.err;
   const int total_blocks = static_cast<int>(Kp / kTcBK);
   if (p.super_k >= K) {
@@ -357,11 +400,16 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   st = cuda_status(counted(launch_scale(C, ldc, t.M, t.N, beta, stream)));
   if (st == PHOBOS_OK && mark(g_ev_start, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
   const int chunk_blocks = static_cast<int>(p.super_k / kTcBK);
-  for (int kb = 0; st == PHOBOS_OK && kb < total_blocks; kb += chunk_blocks) {
+  for (int kb = 0; st == PHOBOS_OK && kb < total_blocks; kb += chunk_blocks, ++t.epoch) {
     t.alpha = alpha;
     t.beta = 1.0f;
     t.k_block0 = kb;
     t.k_blocks = total_blocks - kb < chunk_blocks ? total_blocks - kb : chunk_blocks;
+    // a short last chunk may not afford as many pieces
+    if (t.tail_split > 1 && t.tail_split > t.k_blocks / kMinPieceBlocks) {
+      t.tail_split = t.k_blocks / kMinPieceBlocks >= 2 ? t.k_blocks / kMinPieceBlocks : 1;
+      if (t.tail_split == 1) t.full_tiles = total_tiles;
+    }
     st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream)
                                    : launch_tc(t, passes, bn, p.stages, stream)));
   }

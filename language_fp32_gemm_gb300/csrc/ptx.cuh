@@ -15,6 +15,7 @@ enum : int {
   kDevTimeoutMma = 0x102,
   kDevTimeoutEpilogue = 0x103,
   kDevTimeoutDrain = 0x104,
+  kDevTimeoutPartial = 0x105,
 };
 
 // A wait gives up after this much wall time (nanoseconds, %globaltimer).
@@ -317,6 +318,18 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       " [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
+}
+
+// ------------------------------------------------- global flags between CTAs
+
+__device__ __forceinline__ void st_release_gpu(unsigned *addr, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *addr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
 }
 
 // ------------------------------------------------------------------- convert

@@ -93,6 +93,38 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
   tn = r / rows;
 }
 
+// One unit of work of a persistent CTA (pair): a whole tile, or one K piece of
+// a tile of the last wave (piece >= 0).
+struct Unit {
+  int tile, k_lo, k_hi, piece;
+};
+
+// The i-th unit of worker w out of `units`: whole tiles w, w + units, ... below
+// full_tiles, then at most one K piece of a tail tile.  Every role of the CTA
+// walks the same sequence.
+__device__ __forceinline__ bool unit_of(const TcArgs &p, int w, int units, int i, Unit &u) {
+  const int total = p.tiles_m * p.tiles_n;
+  if (p.tail_split <= 1) {
+    const int t = w + i * units;
+    if (t >= total) return false;
+    u = Unit{t, 0, p.k_blocks, -1};
+    return true;
+  }
+  const int n_whole = p.full_tiles > w ? (p.full_tiles - w + units - 1) / units : 0;
+  if (i < n_whole) {
+    u = Unit{w + i * units, 0, p.k_blocks, -1};
+    return true;
+  }
+  const int S = p.tail_split;
+  if (i > n_whole || w >= (total - p.full_tiles) * S) return false;
+  const int piece = w % S;
+  u.tile = p.full_tiles + w / S;
+  u.piece = piece;
+  u.k_lo = static_cast<int>(static_cast<long long>(p.k_blocks) * piece / S);
+  u.k_hi = static_cast<int>(static_cast<long long>(p.k_blocks) * (piece + 1) / S);
+  return true;
+}
+
 template <int BN, int PASSES, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
@@ -127,9 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   constexpr int kTileM = PAIR ? 2 * kBM : kBM;
   const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  const int total_tiles = p.tiles_m * p.tiles_n;
   const int chunk = p.promote_blocks;
-  const int n_chunks = (p.k_blocks + chunk - 1) / chunk;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -176,12 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
       uint32_t armed = 0, last_parity = 0;
       int g = 0;  // k blocks loaded so far by this CTA: ring slot and phase
       bool ok = true;
-      for (int t = unit; t < total_tiles && ok; t += units) {
+      Unit u;
+      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
         int tm, tn;
-        raster(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
         const int m0 = tm * kTileM + static_cast<int>(rank) * kBM;
         const int b_row = tn * BN + static_cast<int>(rank) * S::kBRows;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++g) {
+        for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1u;
           // Failure-detection test: the first stage is never loaded, so the
@@ -237,8 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
       int g = 0;       // k blocks consumed: ring slot and phase
       int c_glob = 0;  // partial sums produced: TMEM buffer and its phase
       bool ok = true;
-      for (int t = unit; t < total_tiles && ok; t += units) {
-        int kb = 0;
+      Unit u;
+      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+        int kb = u.k_lo;
+        const int n_chunks = (u.k_hi - u.k_lo + chunk - 1) / chunk;
         for (int c = 0; c < n_chunks && ok; ++c, ++c_glob) {
           const int b = c_glob & 1;
           const uint32_t use = static_cast<uint32_t>(c_glob >> 1);
@@ -256,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-          const int kb_end = min(p.k_blocks, kb + chunk);
+          const int kb_end = min(u.k_hi, kb + chunk);
           for (int first = 1; kb < kb_end; ++kb, ++g, first = 0) {
             const int s = g % STAGES;
             const uint32_t ph = (g / STAGES) & 1u;
@@ -322,12 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int c_glob = 0;
     bool ok = true;
-    for (int t = unit; t < total_tiles && ok; t += units) {
+    Unit u;
+    for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
       int tm, tn;
-      raster(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
       float sum[kHalf];
 #pragma unroll
       for (int j = 0; j < kHalf; ++j) sum[j] = 0.f;
+      const int n_chunks = (u.k_hi - u.k_lo + chunk - 1) / chunk;
       for (int c = 0; c < n_chunks; ++c, ++c_glob) {
         const int b = c_glob & 1;
         const uint32_t use = static_cast<uint32_t>(c_glob >> 1);
@@ -356,9 +391,62 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
         }
       }
       if (!ok) break;
+      // Tail pieces: this thread's 1 x kHalf slice of the tile in slot order.
+      const int tile_row = static_cast<int>(rank) * kBM + q * 32 + lane;  // 0 .. kTileM-1
+      if (u.piece > 0) {
+        // Hand the partial sum to the piece-0 owner through L2, then release
+        // the flag once every accumulator thread's stores are visible.
+        const long long slot = static_cast<long long>(u.tile - p.full_tiles) * (p.tail_split - 1) +
+                               (u.piece - 1);
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.partials + (slot * kTileM + tile_row) * BN + h * kHalf);
+#pragma unroll
+        for (int v = 0; v < kHalf / 4; ++v)
+          __stcg(dst + v, make_float4(sum[4 * v], sum[4 * v + 1], sum[4 * v + 2], sum[4 * v + 3]));
+        // Each warp publishes its own slice: no CTA-wide barrier, so a warp
+        // that left on an abort path cannot strand the others.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          st_release_gpu(p.flags + (slot * 2 + rank) * kEpiWarps + (warp - 2), p.epoch);
+        continue;
+      }
+      if (u.piece == 0) {
+        // Owner: add the other pieces in piece order (deterministic).
+        for (int pc = 1; pc < p.tail_split && ok; ++pc) {
+          const long long slot =
+              static_cast<long long>(u.tile - p.full_tiles) * (p.tail_split - 1) + (pc - 1);
+          const unsigned *flag = p.flags + (slot * 2 + rank) * kEpiWarps + (warp - 2);
+          if (ld_acquire_gpu(flag) != p.epoch) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t polls = 1; ld_acquire_gpu(flag) != p.epoch; ++polls) {
+              if ((polls & 31u) == 0 &&
+                  (*abort_flag || polls >= kWaitLimitPolls || globaltimer_ns() - t0 > kWaitLimitNs)) {
+                if (!*abort_flag) atomicCAS(p.err, 0, kDevTimeoutPartial);
+                *abort_flag = 1;
+                abort_peer();
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (!ok) break;
+          const float4 *src = reinterpret_cast<const float4 *>(
+              p.partials + (slot * kTileM + tile_row) * BN + h * kHalf);
+#pragma unroll
+          for (int v = 0; v < kHalf / 4; ++v) {
+            const float4 x = __ldcg(src + v);
+            sum[4 * v + 0] = __fadd_rn(sum[4 * v + 0], x.x);
+            sum[4 * v + 1] = __fadd_rn(sum[4 * v + 1], x.y);
+            sum[4 * v + 2] = __fadd_rn(sum[4 * v + 2], x.z);
+            sum[4 * v + 3] = __fadd_rn(sum[4 * v + 3], x.w);
+          }
+        }
+        if (!ok) break;
+      }
       // The tile's sum is in registers: TMEM already serves the next tile's
       // MMAs while this store runs.
-      const int row = tm * kTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
+      const int row = tm * kTileM + tile_row;
       const int col0 = tn * BN + h * kHalf;
       if (row < p.M && col0 < p.N) {
         float *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
@@ -419,7 +507,9 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   const long long tiles = static_cast<long long>(a.tiles_m) * a.tiles_n;
   // one CTA (pair) per SM (pair), never more than there are tiles
   const long long workers = PAIR ? a.sm_count / 2 : a.sm_count;
-  const unsigned units = static_cast<unsigned>(tiles < workers ? tiles : workers);
+  const unsigned units = a.grid_units > 0
+                             ? static_cast<unsigned>(a.grid_units)
+                             : static_cast<unsigned>(tiles < workers ? tiles : workers);
   if (units == 0) return cudaErrorInvalidValue;
   if (!PAIR) {
     kern<<<units, kThreads, smem, stream>>>(a);

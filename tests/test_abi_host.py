@@ -80,7 +80,7 @@ def test_plan_paths(lib):
     assert p.path == phobos.PHOBOS_PATH_3XTF32
     assert p.tile_m == 256 and p.cluster_m == 2 and p.tile_n == 256 and p.tile_k == 32
     assert p.stages >= 2
-    assert p.super_k == 8192 and p.super_m == 4096
+    assert p.super_k == 8192 and p.super_m == 4096 and p.tail_split == 0
     # split operands: (Mp + Np) * Kp * 4 bytes, big and small
     assert p.workspace_bytes == 2 * (8192 + 8192) * 8192 * 4
     p = phobos.phobos_gemm_plan(8192, 8192, 8192, 8192, 8192, 8192, "tf32")

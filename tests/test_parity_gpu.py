@@ -199,3 +199,37 @@ def test_timing_events_and_launch_count(dev):
     torch.cuda.synchronize()
     assert phobos.phobos_kernel_launches() - n0 == 3  # split A, split B, main kernel
     assert start.elapsed_time(stop) > 0
+
+
+# ------------------------------------------------------- tail split along K
+
+@pytest.mark.parametrize("math", ["3xtf32", "tf32"])
+@pytest.mark.parametrize("shape,split,super_k", [
+    ((512, 512, 2048), 0, None),     # 4 pair tiles: automatic split over idle SMs
+    ((512, 512, 2048), 1, None),     # split switched off
+    ((512, 512, 2048), 3, None),     # forced, uneven K pieces
+    ((1000, 100, 1024), 0, None),    # single-CTA tiles (N <= 128)
+    ((520, 390, 2100), 0, 512),      # split inside every K chunk of the cluster split
+    ((777, 1290, 333), 0, None),     # ragged edges, short K: pieces of at least 4 blocks
+], ids=lambda v: str(v))
+def test_tail_split(dev, math, shape, split, super_k):
+    M, N, K = shape
+    plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, math)
+    plan.tail_split = split
+    if super_k is not None:
+        plan.super_k = super_k
+    A = si.normal(81, 0, (M, K))
+    B = si.normal(81, 1, (K, N))
+    C0 = si.uniform_pm1(81, 2, (M, N))
+    C1, _, _ = check(dev, A, B, C0, 0.5, 1.5, math, plan=plan)
+    # deterministic: the same call again gives the same bits
+    C2 = run_gemm(torch, dev, A, B, C0, 0.5, 1.5, math, plan=plan)
+    assert np.array_equal(C1, C2)
+
+
+def test_tail_split_rejects_bad_values(dev):
+    plan = phobos.phobos_gemm_plan(512, 512, 512, 512, 512, 512, "3xtf32")
+    plan.tail_split = 9
+    A = torch.zeros(512, 512, device=dev)
+    with pytest.raises(phobos.PhobosError):
+        phobos.sgemm(A, A, A.clone(), 1.0, 0.0, math="3xtf32", plan=plan)
