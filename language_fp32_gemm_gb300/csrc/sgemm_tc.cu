@@ -29,8 +29,10 @@
 //    TMEM double buffering.  The tile's final sum therefore lives in registers
 //    (128 lanes x BN columns spread over 256 threads), the same place the
 //    pages' codegen puts a CTA-wide accumulator tile.
-//  - Epilogue: fmaf(alpha, sum, beta * c_old) with 16-byte vector loads and
-//    stores where C allows and scalar edge handling.
+//  - Epilogue: fmaf(alpha, sum, beta * c_old).  Aligned C takes 16-byte
+//    row-segment stores; any other ldc or edge goes through a per-warp 32 x 32
+//    shared-memory transpose so every access is a coalesced row segment.  The
+//    old C values of a block are loaded before any store.
 //
 //  - CTA pairs (PAIR = true): a thread-block cluster of two CTAs on the two
 //    SMs of one TPC computes a 256 x BN tile with tcgen05.mma.cta_group::2
@@ -74,7 +76,8 @@ struct TcShape {
   static constexpr int kBTile = kBRows * kBK * 4;
   static constexpr int kStageBytes = kOps * (kATile + kBTile);
   static constexpr int kTmemCols = 2 * BN;            // two accumulator buffers
-  static constexpr int kAux = 1024 + 256;             // alignment slack + barriers
+  // alignment slack + barriers + the accumulator warps' 32 x 32 transpose buffers
+  static constexpr int kAux = 1024 + 256 + kEpiWarps * 32 * 32 * 4;
   static constexpr int max_stages() { return (kSmemLimit - kAux) / kStageBytes; }
   static constexpr int smem_bytes(int stages) { return stages * kStageBytes + kAux; }
 };
@@ -137,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   // bars: [0,S) full, [S,2S) empty, 2S+{0,1} acc_full, 2S+{2,3} acc_empty, 2S+4 MMA drained
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *epi_stage = reinterpret_cast<float *>(aux + 256);  // kEpiWarps x 32 x 32 floats
 
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8u * STAGES;
@@ -445,37 +449,74 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
         if (!ok) break;
       }
       // The tile's sum is in registers: TMEM already serves the next tile's
-      // MMAs while this store runs.
+      // MMAs while this store runs.  The old C values of a block are all
+      // loaded before any store, so the loads overlap instead of waiting on
+      // one another.
       const int row = tm * kTileM + tile_row;
       const int col0 = tn * BN + h * kHalf;
-      if (row < p.M && col0 < p.N) {
-        float *crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
-        const float alpha = p.alpha, beta = p.beta;
-        if (p.vec_c && col0 + kHalf <= p.N) {
-          float4 *dst = reinterpret_cast<float4 *>(crow);
+      const float alpha = p.alpha, beta = p.beta;
+      if (p.vec_c && col0 + kHalf <= p.N) {  // warp-uniform
+        // Aligned C: each thread writes its row segment with 16-byte stores.
+        if (row < p.M) {
+          float4 *dst = reinterpret_cast<float4 *>(p.C + static_cast<int64_t>(row) * p.ldc + col0);
 #pragma unroll
-          for (int v = 0; v < kHalf / 4; ++v) {
-            float4 o;
+          for (int v0 = 0; v0 < kHalf / 4; v0 += 4) {
+            float4 old[4];
             if (beta != 0.0f) {
-              const float4 old = dst[v];
-              o.x = fmaf(alpha, sum[4 * v + 0], beta * old.x);
-              o.y = fmaf(alpha, sum[4 * v + 1], beta * old.y);
-              o.z = fmaf(alpha, sum[4 * v + 2], beta * old.z);
-              o.w = fmaf(alpha, sum[4 * v + 3], beta * old.w);
-            } else {
-              o.x = alpha * sum[4 * v + 0];
-              o.y = alpha * sum[4 * v + 1];
-              o.z = alpha * sum[4 * v + 2];
-              o.w = alpha * sum[4 * v + 3];
-            }
-            dst[v] = o;
-          }
-        } else {
 #pragma unroll
-          for (int j = 0; j < kHalf; ++j) {
-            if (col0 + j < p.N)
-              crow[j] = beta != 0.0f ? fmaf(alpha, sum[j], beta * crow[j]) : alpha * sum[j];
+              for (int i = 0; i < 4; ++i) old[i] = dst[v0 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int v = v0 + i;
+              float4 o;
+              if (beta != 0.0f) {
+                o.x = fmaf(alpha, sum[4 * v + 0], beta * old[i].x);
+                o.y = fmaf(alpha, sum[4 * v + 1], beta * old[i].y);
+                o.z = fmaf(alpha, sum[4 * v + 2], beta * old[i].z);
+                o.w = fmaf(alpha, sum[4 * v + 3], beta * old[i].w);
+              } else {
+                o.x = alpha * sum[4 * v + 0];
+                o.y = alpha * sum[4 * v + 1];
+                o.z = alpha * sum[4 * v + 2];
+                o.w = alpha * sum[4 * v + 3];
+              }
+              dst[v] = o;
+            }
           }
+        }
+      } else {
+        // Any ldc, alignment or edge: the warp transposes 32 x 32 blocks through
+        // shared memory (XOR-swizzled, conflict-free), so each load and store
+        // instruction covers 32 consecutive columns of one row.
+        const int row0 = row - lane;
+        float *sbuf = epi_stage + (warp - 2) * 32 * 32;
+#pragma unroll
+        for (int j0 = 0; j0 < kHalf; j0 += 32) {
+          const int col = col0 + j0 + lane;
+          if (col0 + j0 >= p.N) break;  // uniform across the warp
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sbuf[lane * 32 + (j ^ lane)] = sum[j0 + j];
+          __syncwarp();
+#pragma unroll 1
+          for (int r0 = 0; r0 < 32; r0 += 8) {
+            float old[8];
+            if (beta != 0.0f) {
+#pragma unroll
+              for (int r = 0; r < 8; ++r)
+                old[r] = (row0 + r0 + r < p.M && col < p.N)
+                             ? p.C[static_cast<int64_t>(row0 + r0 + r) * p.ldc + col]
+                             : 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const float v = sbuf[(r0 + r) * 32 + (lane ^ (r0 + r))];
+              if (row0 + r0 + r < p.M && col < p.N)
+                p.C[static_cast<int64_t>(row0 + r0 + r) * p.ldc + col] =
+                    beta != 0.0f ? fmaf(alpha, v, beta * old[r]) : alpha * v;
+            }
+          }
+          __syncwarp();
         }
       }
     }
