@@ -86,7 +86,8 @@ typedef enum {
  *  super_k         K chunk of the cluster split: super_k < K runs an init
  *                  leaf C = beta*C then one step leaf C += alpha*A_c*B_c per
  *                  chunk (results equal up to rounding order).
- *  workspace_bytes device workspace of the operand pre-pass (the tail split
+ *  workspace_bytes device workspace of the operand pre-pass, for A and B
+ *                  (less when A is split inside the kernel; the tail split
  *                  below adds at most one tile of partial sums per CTA pair,
  *                  about 20 MB on GB300, plus flags).
  *  tail_split      tensor-core paths: K pieces for each tile of the last,
@@ -94,6 +95,13 @@ typedef enum {
  *                  tail (0 = chosen from the SM count, 1 = off, 2..8 = that
  *                  many, capped so every piece spans at least K = 128).
  *                  Results are equal up to rounding order and deterministic.
+ *  a_split         tensor-core paths: where A is split into tf32 big/small
+ *                  (0 = chosen per call: inside the kernel when N <= 1024 and
+ *                  A's rows are 16-byte aligned, where a separate pass over A
+ *                  would cost a large share of the GEMM; 1 = a pre-pass into
+ *                  the workspace; 2 = inside the kernel, which needs
+ *                  lda % 4 == 0 and a 16-byte-aligned A, else
+ *                  PHOBOS_ERR_UNSUPPORTED).  Identical results either way.
  */
 typedef struct {
   int32_t path;
@@ -104,6 +112,7 @@ typedef struct {
   int64_t super_m, super_n, super_k;
   size_t workspace_bytes;
   int32_t tail_split;
+  int32_t a_split;
 } phobos_gemm_plan_t;
 
 /*

@@ -56,7 +56,7 @@ class PhobosGemmPlan(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("multicast", ctypes.c_int32),
                 ("super_m", ctypes.c_int64), ("super_n", ctypes.c_int64),
                 ("super_k", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t),
-                ("tail_split", ctypes.c_int32)]
+                ("tail_split", ctypes.c_int32), ("a_split", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

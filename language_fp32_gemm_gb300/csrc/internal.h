@@ -55,6 +55,10 @@ struct TcArgs {
   // + warp - 2]; piece 0 adds the slots in order and stores C.
   int full_tiles, tail_split;
   int grid_units;  // CTAs (pairs) to launch; 0 = min(tiles, SMs (pairs))
+  // 1: tmap_ab maps the caller's raw fp32 A (K x M extents, zero fill outside)
+  // and the kernel splits it into tf32 big/small in shared memory; tmap_as is
+  // unused.  0: both A maps point at the pre-split workspace.
+  int a_inline;
   float *partials;
   unsigned *flags;
   unsigned epoch;

@@ -33,6 +33,9 @@ constexpr int kPromoteBlocks = 8;
 constexpr int kMaxTailSplit = 8;
 constexpr int kMinPieceBlocks = 4;
 constexpr int kEpiWarps = 8;  // accumulator warps of the tensor-core kernel (one flag each)
+// Automatic a_split: split A inside the kernel up to this N (a pre-pass over
+// A costs about 6 * TF32/3-rate / (N * HBM bandwidth) of the GEMM: ~30 % at N = 1024).
+constexpr int64_t kInlineSplitMaxN = 1024;
 
 std::mutex g_mutex;       // planner caches, device state, workspaces
 std::mutex g_host_mutex;  // serialises the host-buffer entry point (shared staging)
@@ -146,6 +149,22 @@ phobos_status_t make_kmajor_map(CUtensorMap *map, const float *base, int64_t row
   return r == CUDA_SUCCESS ? PHOBOS_OK : PHOBOS_ERR_CUDA;
 }
 
+// Tensor map of a caller's row-major matrix read as a K-major operand: `rows`
+// x `k` elements with leading dimension `ld` (a multiple of 4), boxes of 32 x
+// box_rows, 128B swizzle; reads outside the matrix return zeros.
+phobos_status_t make_kmajor_map_strided(CUtensorMap *map, const float *base, int64_t rows,
+                                        int64_t k, int64_t ld, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PHOBOS_OK : PHOBOS_ERR_CUDA;
+}
+
 phobos_status_t check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                             int64_t ldc) {
   if (M < 0 || N < 0 || K < 0) return PHOBOS_ERR_INVALID_VALUE;
@@ -217,6 +236,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
     return PHOBOS_ERR_UNSUPPORTED;
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
   if (p.tail_split < 0 || p.tail_split > kMaxTailSplit) return PHOBOS_ERR_INVALID_VALUE;
+  if (p.a_split < 0 || p.a_split > 2) return PHOBOS_ERR_INVALID_VALUE;
   if (p.path == PHOBOS_PATH_FFMA) {
     if (p.cluster_m != 1) return PHOBOS_ERR_UNSUPPORTED;
     if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
@@ -230,6 +250,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
       return PHOBOS_ERR_INVALID_VALUE;
     const int max_st = pair ? tc_pair_max_stages(passes, p.tile_n) : tc_max_stages(passes, p.tile_n);
     if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
+    if (p.a_split == 2 && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
     if (p.super_k < K && p.super_k % kTcBK != 0) return PHOBOS_ERR_INVALID_VALUE;
     if (round_up(N, p.tile_n) / 32 > 65535) return PHOBOS_ERR_UNSUPPORTED;
   } else {
@@ -295,7 +316,21 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int bm = pair ? 2 * kTcBM : kTcBM;
   const int bn = p.tile_n;
   const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
-  const size_t ops_bytes = tc_workspace(M, N, K, bm, bn, passes);
+  // Where A is split: inside the kernel (TMA reads the caller's A directly)
+  // or by the pre-pass into the workspace.
+  const bool a_tma_ok = (lda % 4 == 0) && aligned16(A);
+  bool a_inline = false;
+  if (p.a_split == 2) {
+    if (!a_tma_ok) return PHOBOS_ERR_UNSUPPORTED;
+    a_inline = true;
+  } else if (p.a_split == 0) {
+    const int max_st = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
+    a_inline = a_tma_ok && N <= kInlineSplitMaxN && p.stages == max_st;
+  }
+  const int64_t a_bytes = round_up(Mp * Kp * 4, 256), b_bytes = round_up(Np * Kp * 4, 256);
+  const int ops = passes == 3 ? 2 : 1;  // big (+ small)
+  // workspace: [B big][B small][A big][A small] (no A part when A is split in-kernel)
+  const size_t ops_bytes = static_cast<size_t>(ops * b_bytes + (a_inline ? 0 : ops * a_bytes));
 
   // Persistent grid: one CTA (pair) per SM (pair).  Split the tiles of the
   // last, partial wave along K so that idle SMs share the tail.
@@ -331,16 +366,17 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   if ((st = get_encoder()) != PHOBOS_OK) return st;
 
   char *base = static_cast<char *>(ws.ptr);
-  const int64_t a_bytes = round_up(Mp * Kp * 4, 256), b_bytes = round_up(Np * Kp * 4, 256);
-  float *a_big = reinterpret_cast<float *>(base);
-  float *a_small = passes == 3 ? reinterpret_cast<float *>(base + a_bytes) : nullptr;
-  float *b_big = reinterpret_cast<float *>(base + (passes == 3 ? 2 : 1) * a_bytes);
-  float *b_small = passes == 3 ? reinterpret_cast<float *>(base + 2 * a_bytes + b_bytes) : nullptr;
+  float *b_big = reinterpret_cast<float *>(base);
+  float *b_small = passes == 3 ? reinterpret_cast<float *>(base + b_bytes) : nullptr;
+  float *a_big = reinterpret_cast<float *>(base + ops * b_bytes);
+  float *a_small = passes == 3 ? reinterpret_cast<float *>(base + ops * b_bytes + a_bytes) : nullptr;
 
-  st = cuda_status(counted(launch_split_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
-                                     static_cast<int>(Mp), static_cast<int>(Kp), a_big, a_small,
-                                     (lda % 4 == 0) && aligned16(A), stream)));
-  if (st != PHOBOS_OK) return st;
+  if (!a_inline) {
+    st = cuda_status(counted(launch_split_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
+                                               static_cast<int>(Mp), static_cast<int>(Kp), a_big,
+                                               a_small, a_tma_ok, stream)));
+    if (st != PHOBOS_OK) return st;
+  }
   st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
                                              static_cast<int>(Np), static_cast<int>(Kp), b_big,
                                              b_small, stream)));
@@ -349,15 +385,21 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   TcArgs t{};
   // each CTA loads 128 rows of A and, in a pair, half of the tile's B rows
   const int b_box = pair ? bn / 2 : bn;
-  if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
-  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, b_box)) != PHOBOS_OK) return st;
-  if (passes == 3) {
-    if ((st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
-    if ((st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, b_box)) != PHOBOS_OK) return st;
-  } else {
+  if (a_inline) {
+    // the caller's A: K x M extents with its own stride; TMA fills zeros outside
+    if ((st = make_kmajor_map_strided(&t.tmap_ab, A, M, K, lda, kTcBM)) != PHOBOS_OK) return st;
     t.tmap_as = t.tmap_ab;
-    t.tmap_bs = t.tmap_bb;
+  } else {
+    if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
+    t.tmap_as = t.tmap_ab;
+    if (passes == 3 && (st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, kTcBM)) != PHOBOS_OK)
+      return st;
   }
+  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, b_box)) != PHOBOS_OK) return st;
+  t.tmap_bs = t.tmap_bb;
+  if (passes == 3 && (st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, b_box)) != PHOBOS_OK)
+    return st;
+  t.a_inline = a_inline ? 1 : 0;
   t.C = C;
   t.ldc = ldc;
   t.M = static_cast<int>(M);

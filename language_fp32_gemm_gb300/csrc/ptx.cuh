@@ -152,6 +152,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes (32 fp32), eight-row groups
 // 1024 bytes apart.  `addr` must lie in a 1024-byte aligned tile; advancing it
@@ -335,11 +341,13 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *addr) {
 // ------------------------------------------------------------------- convert
 
 // Round to the nearest tf32 value (10 explicit mantissa bits), ties away from
-// zero; the low 13 bits of the result are zero.
-__device__ __forceinline__ float to_tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+// zero, on the IEEE bit pattern: adding half of the dropped range (2^12) to
+// the magnitude bits and clearing the 13 low bits rounds the magnitude to
+// nearest with ties up; a carry moves into the exponent as it should.  Equal to
+// cvt.rna.tf32.f32 for finite values; two integer operations.
+__device__ __forceinline__ float tf32_rna_bits(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
+
 
 }  // namespace phobos

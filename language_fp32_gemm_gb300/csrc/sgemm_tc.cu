@@ -51,7 +51,10 @@
 // warps still store the previous tile from registers.
 //
 // Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
-// MMA issuer, warps 2..9 = accumulator/epilogue warps.  Epilogue warp w reads
+// MMA issuer, warps 2..9 = accumulator/epilogue warps; with A split inside the
+// kernel (384 threads), the producer TMA-loads the caller's raw fp32 A (zero
+// fill outside the matrix) and warps 10 and 11 split each landed tile in place
+// into tf32 big/small before the MMA issuer may use it.  Epilogue warp w reads
 // TMEM lanes 32*(w%4) .. +31 (the hardware's lane-quarter rule) and columns
 // [h*BN/2, (h+1)*BN/2) with h = (w-2)/4.
 #include "internal.h"
@@ -65,6 +68,8 @@ constexpr int kBM = 128;  // A rows (and output rows) per CTA
 constexpr int kBK = 32;   // fp32 elements per row of one stage = 128 bytes = swizzle span
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kCvtWarps = 2;  // warps 10, 11: split A in shared memory (in-kernel A split)
+constexpr int threads_for(bool asplit) { return kThreads + (asplit ? 32 * kCvtWarps : 0); }
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint64_t kAbortGraceNs = 200000;  // let copies in flight land before exit
 
@@ -128,8 +133,9 @@ __device__ __forceinline__ bool unit_of(const TcArgs &p, int w, int units, int i
   return true;
 }
 
-template <int BN, int PASSES, int STAGES, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT>
+__global__ void __launch_bounds__(threads_for(ASPLIT), 1)
+    sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
   constexpr int kHalf = BN / 2;  // columns summed by one epilogue thread
   extern __shared__ uint8_t smem_raw[];
@@ -137,8 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   const uint32_t tiles = (raw + 1023u) & ~1023u;  // 1024-byte aligned stage ring
   uint8_t *aux = smem_raw + (tiles - raw) + STAGES * S::kStageBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(aux);
-  // bars: [0,S) full, [S,2S) empty, 2S+{0,1} acc_full, 2S+{2,3} acc_empty, 2S+4 MMA drained
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+  // bars: [0,S) full, [S,2S) empty, 2S+{0,1} acc_full, 2S+{2,3} acc_empty, 2S+4 MMA drained,
+  // then (in-kernel A split) [2S+5, 3S+5) a_full, [3S+5, 4S+5) converted
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * STAGES + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   float *epi_stage = reinterpret_cast<float *>(aux + 256);  // kEpiWarps x 32 x 32 floats
 
@@ -147,6 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   const uint32_t acc_full0 = full0 + 16u * STAGES;
   const uint32_t acc_empty0 = acc_full0 + 16u;
   const uint32_t mma_drained = acc_full0 + 32u;
+  const uint32_t a_full0 = mma_drained + 8u;     // this CTA's raw A tile landed
+  const uint32_t conv0 = a_full0 + 8u * STAGES;  // A tile split (leader: both CTAs)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -175,6 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
       mbar_init(acc_empty0 + 8u * b, (PAIR ? 2 : 1) * kEpiWarps);
     }
     mbar_init(mma_drained, 1);
+    if (ASPLIT) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(a_full0 + 8u * s, 1);
+        mbar_init(conv0 + 8u * s, (PAIR ? 2 : 1) * kCvtWarps);
+      }
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -204,7 +219,111 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp >= 2 + kEpiWarps) {
+    // --------------------------------------- A-split warps (in-kernel split)
+    // Each of the two warps converts half of every landed raw A tile in place:
+    // big = rna_tf32(x) over x, small = rna_tf32(x - big) into the second A slot
+    // at the same (swizzled) offset, then tells the MMA issuer (of the pair's
+    // leader) that its half is ready.
+    const int cw = warp - 2 - kEpiWarps;
+    constexpr int kPerWarp = S::kATile / 16 / kCvtWarps;  // float4s per warp and stage
+    int g = 0;
+    bool ok = true;
+    Unit u;
+    for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+      for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1u;
+        if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+        if (!bounded_wait(a_full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutProducer)) {
+          abort_peer();
+          ok = false;
+          break;
+        }
+        float4 *big = reinterpret_cast<float4 *>(smem_raw + (tiles - raw) + s * S::kStageBytes) +
+                      cw * kPerWarp;
+        float4 *small = big + S::kATile / 16;
+#pragma unroll 8
+        for (int j = 0; j < kPerWarp / 32; ++j) {
+          const int idx = j * 32 + lane;
+          const float4 x = big[idx];
+          float4 b, sm;
+          b.x = tf32_rna_bits(x.x); sm.x = tf32_rna_bits(x.x - b.x);
+          b.y = tf32_rna_bits(x.y); sm.y = tf32_rna_bits(x.y - b.y);
+          b.z = tf32_rna_bits(x.z); sm.z = tf32_rna_bits(x.z - b.z);
+          b.w = tf32_rna_bits(x.w); sm.w = tf32_rna_bits(x.w - b.w);
+          big[idx] = b;
+          if (PASSES == 3) small[idx] = sm;
+        }
+        fence_proxy_async_shared();  // the tensor core reads these through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(mapa_shared(conv0 + 8u * s, 0));
+          else
+            mbar_arrive(conv0 + 8u * s);
+        }
+      }
+    }
+  } else if (warp == 0 && ASPLIT) {
+    // --------------------------- producer when A is split inside the kernel
+    if (lane == 0) {
+      uint32_t armed = 0, last_parity = 0;
+      int g = 0;
+      bool ok = true;
+      Unit u;
+      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+        int tm, tn;
+        raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        const int m0 = tm * kTileM + static_cast<int>(rank) * kBM;
+        const int b_row = tn * BN + static_cast<int>(rank) * S::kBRows;
+        for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1u;
+          if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+          if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
+            abort_peer();
+            ok = false;
+            break;
+          }
+          const uint32_t full = full0 + 8u * s;
+          const uint32_t af = a_full0 + 8u * s;
+          const int kc = (p.k_block0 + kb) * kBK;
+          const uint32_t st = tiles + s * S::kStageBytes;
+          const uint32_t bt = st + S::kOps * S::kATile;
+          mbar_arrive_expect_tx(af, S::kATile);
+          tma_load_2d(st, &p.tmap_ab, af, kc, m0);  // raw A, zero outside the matrix
+          if (PAIR) {
+            if (leader) mbar_arrive_expect_tx(full, 2 * S::kOps * S::kBTile);
+            const uint32_t lead_full = mapa_shared(full, 0);
+            tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
+            if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
+          } else {
+            mbar_arrive_expect_tx(full, S::kOps * S::kBTile);
+            tma_load_2d(bt, &p.tmap_bb, full, kc, b_row);
+            if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, b_row);
+          }
+          armed |= 1u << s;
+          last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        }
+      }
+      // No bulk copy may still be writing shared memory at exit: this CTA's A
+      // loads complete on its own barriers, B loads on the leader's.
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) {
+          bounded_wait(a_full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
+                       kDevTimeoutDrain, false);
+          if (leader)
+            bounded_wait(full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
+                         kDevTimeoutDrain, false);
+        }
+      if (PAIR && *abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kAbortGraceNs) {
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t armed = 0, last_parity = 0;
@@ -297,7 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
           for (int first = 1; kb < kb_end; ++kb, ++g, first = 0) {
             const int s = g % STAGES;
             const uint32_t ph = (g / STAGES) & 1u;
-            if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) {
+            if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma) ||
+                (ASPLIT && !(PAIR ? bounded_wait_cluster(conv0 + 8u * s, ph, abort_flag, p.err,
+                                                         kDevTimeoutMma)
+                                  : bounded_wait(conv0 + 8u * s, ph, abort_flag, p.err,
+                                                 kDevTimeoutMma)))) {
               ok = false;
               abort_peer();
               break;
@@ -537,11 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_tc_kernel(const __grid_cons
   }
 }
 
-template <int BN, int PASSES, int STAGES, bool PAIR>
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT>
 cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
-  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR>;
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT>;
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -553,12 +676,12 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
                              : static_cast<unsigned>(tiles < workers ? tiles : workers);
   if (units == 0) return cudaErrorInvalidValue;
   if (!PAIR) {
-    kern<<<units, kThreads, smem, stream>>>(a);
+    kern<<<units, threads_for(ASPLIT), smem, stream>>>(a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * units, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_for(ASPLIT), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -574,9 +697,12 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
 template <int BN, int PASSES, bool PAIR>
 cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream) {
   constexpr int kMax = TcShape<BN, PASSES, PAIR>::max_stages();
-  if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2), PAIR>(a, stream);
-  if (stages >= 3 && kMax >= 3) return launch_one<BN, PASSES, (kMax >= 3 ? 3 : 2), PAIR>(a, stream);
-  if (stages >= 2) return launch_one<BN, PASSES, 2, PAIR>(a, stream);
+  constexpr int kTop = kMax >= 4 ? 4 : kMax;
+  // In-kernel A split: always the deepest ring.
+  if (a.a_inline) return launch_one<BN, PASSES, kTop, PAIR, true>(a, stream);
+  if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2), PAIR, false>(a, stream);
+  if (stages >= 3 && kMax >= 3) return launch_one<BN, PASSES, (kMax >= 3 ? 3 : 2), PAIR, false>(a, stream);
+  if (stages >= 2) return launch_one<BN, PASSES, 2, PAIR, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 

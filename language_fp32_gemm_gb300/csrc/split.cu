@@ -40,10 +40,10 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float *__restrict
       }
     }
     float4 b, s;
-    b.x = to_tf32_rna(x[0]); s.x = to_tf32_rna(x[0] - b.x);
-    b.y = to_tf32_rna(x[1]); s.y = to_tf32_rna(x[1] - b.y);
-    b.z = to_tf32_rna(x[2]); s.z = to_tf32_rna(x[2] - b.z);
-    b.w = to_tf32_rna(x[3]); s.w = to_tf32_rna(x[3] - b.w);
+    b.x = tf32_rna_bits(x[0]); s.x = tf32_rna_bits(x[0] - b.x);
+    b.y = tf32_rna_bits(x[1]); s.y = tf32_rna_bits(x[1] - b.y);
+    b.z = tf32_rna_bits(x[2]); s.z = tf32_rna_bits(x[2] - b.z);
+    b.w = tf32_rna_bits(x[3]); s.w = tf32_rna_bits(x[3] - b.w);
     const int64_t o = static_cast<int64_t>(i) * Kp + k;
     *reinterpret_cast<float4 *>(big + o) = b;
     if (small) *reinterpret_cast<float4 *>(small + o) = s;
@@ -72,10 +72,10 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float *__restrict
     const int n = n0 + ty + r;
     const int k = k0 + tx;
     const float x = tile[tx][ty + r];
-    const float b = to_tf32_rna(x);
+    const float b = tf32_rna_bits(x);
     const int64_t o = static_cast<int64_t>(n) * Kp + k;
     big[o] = b;
-    if (small) small[o] = to_tf32_rna(x - b);
+    if (small) small[o] = tf32_rna_bits(x - b);
   }
 }
 

@@ -190,15 +190,18 @@ def test_timing_events_and_launch_count(dev):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()  # torch creates the CUDA events lazily, on first record
     stop.record()
-    n0 = phobos.phobos_kernel_launches()
-    phobos.phobos_set_timing_events(start.cuda_event, stop.cuda_event)
-    try:
-        phobos.sgemm(A, B, C, 1.0, 0.0, math="3xtf32")
-    finally:
-        phobos.phobos_set_timing_events(None, None)
-    torch.cuda.synchronize()
-    assert phobos.phobos_kernel_launches() - n0 == 3  # split A, split B, main kernel
-    assert start.elapsed_time(stop) > 0
+    for a_split, launches in ((1, 3), (2, 2)):  # (split A,) split B, main kernel
+        plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
+        plan.a_split = a_split
+        n0 = phobos.phobos_kernel_launches()
+        phobos.phobos_set_timing_events(start.cuda_event, stop.cuda_event)
+        try:
+            phobos.sgemm(A, B, C, 1.0, 0.0, math="3xtf32", plan=plan)
+        finally:
+            phobos.phobos_set_timing_events(None, None)
+        torch.cuda.synchronize()
+        assert phobos.phobos_kernel_launches() - n0 == launches
+        assert start.elapsed_time(stop) > 0
 
 
 # ------------------------------------------------------- tail split along K
@@ -233,3 +236,34 @@ def test_tail_split_rejects_bad_values(dev):
     A = torch.zeros(512, 512, device=dev)
     with pytest.raises(phobos.PhobosError):
         phobos.sgemm(A, A, A.clone(), 1.0, 0.0, math="3xtf32", plan=plan)
+
+
+# ---------------------------------------------- A split inside the kernel
+
+@pytest.mark.parametrize("math", ["3xtf32", "tf32"])
+@pytest.mark.parametrize("shape", [(300, 260, 200), (1000, 700, 332), (4096, 256, 1000),
+                                   (129, 100, 36), (640, 1024, 4), (333, 257, 68), (77, 900, 4)],
+                         ids=lambda s: "%dx%dx%d" % s)
+def test_a_split_in_kernel_matches_prepass(dev, math, shape):
+    M, N, K = shape
+    A = si.normal(91, 0, (M, K))
+    B = si.normal(91, 1, (K, N))
+    C0 = si.uniform_pm1(91, 2, (M, N))
+    out = {}
+    for mode in (1, 2):
+        plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, math)
+        plan.a_split = mode
+        out[mode], _, _ = check(dev, A, B, C0, 1.25, 0.75, math, plan=plan)
+    # the same tf32 rounding of A either way: identical bits
+    assert np.array_equal(out[1], out[2])
+
+
+def test_a_split_in_kernel_needs_aligned_rows(dev):
+    M, N, K = 64, 64, 33  # lda = 33 is not a multiple of 4
+    plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
+    plan.a_split = 2
+    A = torch.zeros(M, K, device=dev)
+    B = torch.zeros(K, N, device=dev)
+    with pytest.raises(phobos.PhobosError) as e:
+        phobos.sgemm(A, B, torch.zeros(M, N, device=dev), 1.0, 0.0, math="3xtf32", plan=plan)
+    assert e.value.status == phobos.PHOBOS_ERR_UNSUPPORTED
