@@ -90,13 +90,16 @@ typedef enum {
  *                  (less when A is split inside the kernel; the tail split
  *                  below adds at most one tile of partial sums per CTA pair,
  *                  about 20 MB on GB300, plus flags).
- *  tail_split      tensor-core paths: K pieces for each tile of the last,
+ *  tail_split      FFMA path with 64 x 64 tiles: K slices per tile, summed
+ *                  inside a thread-block cluster through distributed shared
+ *                  memory (0 = enough to fill the SMs, 1 = off, 2..8).
+ *                  Tensor-core paths: K pieces for each tile of the last,
  *                  partial wave of the persistent grid, so idle SMs share the
  *                  tail (0 = chosen from the SM count, 1 = off, 2..8 = that
  *                  many, capped so every piece spans at least K = 128).
  *                  Results are equal up to rounding order and deterministic.
  *  a_split         tensor-core paths: where A is split into tf32 big/small
- *                  (0 = chosen per call: inside the kernel when N <= 1024 and
+ *                  (0 = chosen per call: inside the kernel when N <= 512 and
  *                  A's rows are 16-byte aligned, where a separate pass over A
  *                  would cost a large share of the GEMM; 1 = a pre-pass into
  *                  the workspace; 2 = inside the kernel, which needs

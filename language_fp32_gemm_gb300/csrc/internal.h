@@ -21,6 +21,10 @@ struct FfmaArgs {
   int k_begin;     // first k of this launch
   int k_len;       // number of k of this launch
   int vec_a, vec_b, vec_c;  // 16-byte vector access allowed for A / B / C
+  // 64x64 tiles only: K slices per tile (1 = off, 2..8).  The slices of a tile
+  // form one thread-block cluster and are summed through distributed shared
+  // memory by the cluster's rank 0, in rank order.
+  int kslices;
 };
 cudaError_t launch_ffma(const FfmaArgs &a, cudaStream_t stream);
 

@@ -33,9 +33,11 @@ constexpr int kPromoteBlocks = 8;
 constexpr int kMaxTailSplit = 8;
 constexpr int kMinPieceBlocks = 4;
 constexpr int kEpiWarps = 8;  // accumulator warps of the tensor-core kernel (one flag each)
-// Automatic a_split: split A inside the kernel up to this N (a pre-pass over
-// A costs about 6 * TF32/3-rate / (N * HBM bandwidth) of the GEMM: ~30 % at N = 1024).
-constexpr int64_t kInlineSplitMaxN = 1024;
+// Automatic a_split: split A inside the kernel up to this N.  A pre-pass over
+// A costs about 6 * (TF32/3 rate) / (N * HBM bandwidth) of the GEMM time,
+// ~300/N on GB300; splitting inside the kernel slows the main loop by ~50 %
+// (two converter warps), measured on GB300.  They cross near N = 600.
+constexpr int64_t kInlineSplitMaxN = 512;
 
 std::mutex g_mutex;       // planner caches, device state, workspaces
 std::mutex g_host_mutex;  // serialises the host-buffer entry point (shared staging)
@@ -276,9 +278,23 @@ void log_plan(int64_t M, int64_t N, int64_t K, const phobos_gemm_plan_t &p) {
                (long long)p.super_k, p.workspace_bytes);
 }
 
+// K slices per 64x64 FFMA tile (a cluster summed through DSMEM) when there are
+// fewer tiles than SMs: enough clusters to fill the SMs, each slice at least
+// four K blocks of 8.
+int ffma_kslices(int64_t M, int64_t N, int64_t k_len, const phobos_gemm_plan_t &p,
+                 int sm_count) {
+  if (p.tile_m != 64 || p.tail_split == 1) return 1;
+  const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
+  int64_t S = p.tail_split >= 2 ? p.tail_split : (tiles > 0 ? sm_count / tiles : 1);
+  if (S > 8) S = 8;
+  if (S > (k_len + 31) / 32) S = (k_len + 31) / 32;
+  return S >= 2 ? static_cast<int>(S) : 1;
+}
+
 phobos_status_t run_ffma(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                          int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                         int64_t ldc, cudaStream_t stream, const phobos_gemm_plan_t &p) {
+                         int64_t ldc, cudaStream_t stream, const phobos_gemm_plan_t &p,
+                         const DeviceState &dev) {
   FfmaArgs a{};
   a.A = A; a.B = B; a.C = C;
   a.lda = lda; a.ldb = ldb; a.ldc = ldc;
@@ -289,6 +305,7 @@ phobos_status_t run_ffma(int64_t M, int64_t N, int64_t K, float alpha, const flo
   a.vec_c = (ldc % 4 == 0) && aligned16(C);
   if (p.super_k >= K) {
     a.alpha = alpha; a.beta = beta; a.k_begin = 0; a.k_len = static_cast<int>(K);
+    a.kslices = ffma_kslices(M, N, K, p, dev.sm_count);
     if (mark(g_ev_start, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
     phobos_status_t st = cuda_status(counted(launch_ffma(a, stream)));
     if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
@@ -301,6 +318,7 @@ phobos_status_t run_ffma(int64_t M, int64_t N, int64_t K, float alpha, const flo
     a.alpha = alpha; a.beta = 1.0f;
     a.k_begin = static_cast<int>(k0);
     a.k_len = static_cast<int>(K - k0 < p.super_k ? K - k0 : p.super_k);
+    a.kslices = ffma_kslices(M, N, a.k_len, p, dev.sm_count);
     st = cuda_status(counted(launch_ffma(a, stream)));
   }
   if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
@@ -502,7 +520,7 @@ phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const f
   if (!products) {
     st = cuda_status(counted(launch_scale(C, ldc, static_cast<int>(M), static_cast<int>(N), beta, stream)));
   } else if (plan.path == PHOBOS_PATH_FFMA) {
-    st = run_ffma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan);
+    st = run_ffma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev);
   } else {
     st = run_tc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev, device);
   }

@@ -9,7 +9,16 @@
 // 64 x 64 x 8 (64 threads); the pages' tuned winner on their GPU was
 // 64 x 128 x 8.  Any M, N, K and leading dimension is accepted: loads outside
 // the matrix read zero and stores outside it are skipped.
+//
+// Small problems, with fewer tiles than SMs, split K across the CTAs of a
+// thread-block cluster (up to 8): each CTA sums its K slice, leaves the
+// partial tile in its shared memory, and the cluster's rank 0 adds the other
+// ranks' tiles through distributed shared memory, in rank order
+// (deterministic), before the epilogue.  This is the cluster-level reduction
+// of the "Clusters et DSMEM" chapter, section 3.4 (reduce inside the cluster
+// instead of one atomic per block).
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace phobos {
 
@@ -17,7 +26,7 @@ namespace {
 
 constexpr int kBK = 8;
 
-template <int BM, int BN>
+template <int BM, int BN, bool KSPLIT>
 __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const FfmaArgs p) {
   constexpr int NT = (BM / 8) * (BN / 8);
   constexpr int PAD = 4;
@@ -29,8 +38,17 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const F
 
   const int tid = threadIdx.x;
   const int tiles_n = (p.N + BN - 1) / BN;
-  const int tm = blockIdx.x / tiles_n;
-  const int tn = blockIdx.x - tm * tiles_n;
+  const int slice = KSPLIT ? static_cast<int>(cluster_ctarank()) : 0;
+  const int tile = KSPLIT ? static_cast<int>(blockIdx.x) / p.kslices : static_cast<int>(blockIdx.x);
+  const int tm = tile / tiles_n;
+  const int tn = tile - tm * tiles_n;
+  // this CTA's K range (slices are whole multiples of kBK)
+  int k_lo = p.k_begin, k_hi = p.k_begin + p.k_len;
+  if (KSPLIT) {
+    const int per = ((p.k_len + p.kslices - 1) / p.kslices + kBK - 1) / kBK * kBK;
+    k_lo = min(p.k_begin + slice * per, k_hi);
+    k_hi = min(k_lo + per, k_hi);
+  }
   const int m0 = tm * BM, n0 = tn * BN;
   const int tx = tid % (BN / 8);
   const int ty = tid / (BN / 8);
@@ -46,13 +64,13 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const F
       const int kq = (g % (kBK / 4)) * 4;
       const int gi = m0 + row, gk = k0 + kq;
       const float *src = p.A + static_cast<int64_t>(gi) * p.lda + gk;
-      if (gi < p.M && p.vec_a && gk + 3 < p.k_begin + p.k_len) {
+      if (gi < p.M && p.vec_a && gk + 3 < k_hi) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
         a_reg[l][0] = v.x; a_reg[l][1] = v.y; a_reg[l][2] = v.z; a_reg[l][3] = v.w;
       } else {
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-          a_reg[l][t] = (gi < p.M && gk + t < p.k_begin + p.k_len) ? __ldg(src + t) : 0.f;
+          a_reg[l][t] = (gi < p.M && gk + t < k_hi) ? __ldg(src + t) : 0.f;
       }
     }
 #pragma unroll
@@ -62,7 +80,7 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const F
       const int nq = (g % (BN / 4)) * 4;
       const int gk = k0 + k, gj = n0 + nq;
       const float *src = p.B + static_cast<int64_t>(gk) * p.ldb + gj;
-      const bool krow = gk < p.k_begin + p.k_len;
+      const bool krow = gk < k_hi;
       if (krow && p.vec_b && gj + 3 < p.N) {
         const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
         b_reg[l][0] = v.x; b_reg[l][1] = v.y; b_reg[l][2] = v.z; b_reg[l][3] = v.w;
@@ -98,12 +116,12 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const F
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-  const int k_end = p.k_begin + p.k_len;
+  const int k_end = k_hi;
   int buf = 0;
-  load_tiles(p.k_begin);
+  load_tiles(k_lo);
   store_tiles(0);
   __syncthreads();
-  for (int k0 = p.k_begin; k0 < k_end; k0 += kBK) {
+  for (int k0 = k_lo; k0 < k_end; k0 += kBK) {
     const bool more = k0 + kBK < k_end;
     if (more) load_tiles(k0 + kBK);  // global loads in flight during the FMAs
 #pragma unroll
@@ -124,6 +142,40 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const F
       __syncthreads();
       buf ^= 1;
     }
+  }
+
+  if (KSPLIT) {
+    // Cluster reduction of the K slices through distributed shared memory.
+    __shared__ __align__(16) float part[BM * BN];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<float4 *>(&part[r * BN + tx * 4 + h * (BN / 2)]) =
+            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+    }
+    cluster_sync();  // every slice's partial tile is in place
+    if (slice == 0) {
+      for (int rk = 1; rk < p.kslices; ++rk) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t addr =
+                mapa_shared(smem_u32(&part[r * BN + tx * 4 + h * (BN / 2)]), rk);
+            const float4 v = ld_shared_cluster_v4(addr);
+            acc[i][4 * h + 0] += v.x;
+            acc[i][4 * h + 1] += v.y;
+            acc[i][4 * h + 2] += v.z;
+            acc[i][4 * h + 3] += v.w;
+          }
+        }
+      }
+    }
+    cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
+    if (slice != 0) return;
   }
 
   // Epilogue: C = alpha * acc + beta * C_old; beta == 0 does not read C.
@@ -170,11 +222,26 @@ cudaError_t launch_ffma(const FfmaArgs &a, cudaStream_t stream) {
   if (a.tile == 128) {
     const int64_t tiles = static_cast<int64_t>((a.M + 127) / 128) * ((a.N + 127) / 128);
     if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-    sgemm_ffma_kernel<128, 128><<<static_cast<unsigned>(tiles), 256, 0, stream>>>(a);
+    sgemm_ffma_kernel<128, 128, false><<<static_cast<unsigned>(tiles), 256, 0, stream>>>(a);
   } else if (a.tile == 64) {
     const int64_t tiles = static_cast<int64_t>((a.M + 63) / 64) * ((a.N + 63) / 64);
+    if (a.kslices > 1) {
+      if (a.kslices > 8 || tiles * a.kslices > 0x7fffffff) return cudaErrorInvalidValue;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(tiles * a.kslices), 1, 1);
+      cfg.blockDim = dim3(64, 1, 1);
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(a.kslices);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, sgemm_ffma_kernel<64, 64, true>, a);
+    }
     if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-    sgemm_ffma_kernel<64, 64><<<static_cast<unsigned>(tiles), 64, 0, stream>>>(a);
+    sgemm_ffma_kernel<64, 64, false><<<static_cast<unsigned>(tiles), 64, 0, stream>>>(a);
   } else {
     return cudaErrorInvalidValue;
   }

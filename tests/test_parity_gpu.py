@@ -267,3 +267,22 @@ def test_a_split_in_kernel_needs_aligned_rows(dev):
     with pytest.raises(phobos.PhobosError) as e:
         phobos.sgemm(A, B, torch.zeros(M, N, device=dev), 1.0, 0.0, math="3xtf32", plan=plan)
     assert e.value.status == phobos.PHOBOS_ERR_UNSUPPORTED
+
+
+# --------------------------------------- FFMA split-K over a cluster (DSMEM)
+
+@pytest.mark.parametrize("shape,split", [((256, 256, 256), 0), ((256, 256, 256), 1),
+                                         ((100, 70, 1000), 0), ((64, 64, 8), 0),
+                                         ((130, 129, 300), 3), ((200, 300, 77), 8)],
+                         ids=lambda v: str(v))
+def test_ffma_cluster_split_k(dev, shape, split):
+    M, N, K = shape
+    plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "ffma")
+    assert plan.tile_m == 64
+    plan.tail_split = split
+    A = si.normal(95, 0, (M, K))
+    B = si.normal(95, 1, (K, N))
+    C0 = si.uniform_pm1(95, 2, (M, N))
+    C1, _, _ = check(dev, A, B, C0, 0.5, -1.5, "ffma", plan=plan)
+    C2 = run_gemm(torch, dev, A, B, C0, 0.5, -1.5, "ffma", plan=plan)
+    assert np.array_equal(C1, C2)  # deterministic
