@@ -160,9 +160,12 @@ phobos_status_t phobos_sgemm_ex(int64_t M, int64_t N, int64_t K, float alpha,
 /*
  * Host-buffer form: A, B and C are HOST pointers (pinned memory gives the
  * fastest copies).  The call copies A, B (and C when beta != 0) to device
- * buffers owned by the library, runs phobos_sgemm_ex on `stream`, copies C back
- * and synchronizes `stream` before returning.  Same layout and errors as
- * phobos_sgemm_ex, plus PHOBOS_ERR_OUT_OF_MEMORY for the staging buffers.
+ * buffers owned by the library, runs the GEMM on `stream`, copies C back and
+ * synchronizes `stream` before returning.  Problems on the tensor-core path
+ * with M >= 2048 run as up to 8 row bands on two internal copy streams so
+ * that the copies of later bands overlap the compute of earlier ones.  Same
+ * layout and errors as phobos_sgemm_ex, plus PHOBOS_ERR_OUT_OF_MEMORY for
+ * the staging buffers.  Calls are serialised inside the library.
  */
 phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha,
                                   const float *A, int64_t lda, const float *B,

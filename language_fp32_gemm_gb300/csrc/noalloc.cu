@@ -30,7 +30,8 @@ namespace {
 constexpr size_t kHeadBytes = 256;  // status word, padded to keep the operands aligned
 constexpr size_t kScratchBytes = PHOBOS_NOALLOC_SCRATCH_BYTES;
 constexpr int kBM = 128, kBK = 32;
-constexpr int kPromote = 8;
+// K blocks per TMEM partial sum, by K, as the allocating path chooses them.
+int promote_for(int64_t k) { return k <= 128 ? 1 : k <= 512 ? 2 : k <= 2048 ? 4 : 8; }
 constexpr int64_t kSuper = 4096;
 constexpr int kMaxDevices = 64;
 
@@ -177,7 +178,7 @@ extern "C" phobos_status_t phobos_sgemm_noalloc(int64_t M, int64_t N, int64_t K,
       t.alpha = alpha;
       t.beta = beta;
       t.vec_c = (ldc % 4 == 0) && aligned16(C);
-      t.promote_blocks = kPromote;
+      t.promote_blocks = promote_for(K);
       t.sm_count = g_sm_count[dev];
       t.err = status_word;
       st = ok(launch_tc(t, 3, bn, tc_max_stages(3, bn), stream));

@@ -27,8 +27,24 @@ constexpr int kTcBM = 128;
 constexpr int64_t kFfmaMacLimit = int64_t{1} << 25;     // DEFAULT: FFMA up to 32 Mi MACs
 constexpr int64_t kDefaultSuper = 4096;                 // super-tile edge (raster group)
 // K blocks (of 32) summed in TMEM before the partial sum is added into fp32
-// registers with round-to-nearest adds: 8 blocks = K of 256.
-constexpr int kPromoteBlocks = 8;
+// registers with round-to-nearest adds, for split TF32.  The truncation error
+// of one partial is largest relative to sum|a||b| when the whole K spans few
+// partials.  Measured on GB300 (max over 4 M outputs, normal data, bar 2^-20 =
+// 9.5e-7):
+//   partials of 8 blocks: 1.07e-6 at K = 256, 4.9e-7 at K = 1024, 2.4e-7 at K = 4096
+//   partials of 4 blocks: 8.9e-7 at K = 128, 5.6e-7 at K = 256, 2.5e-7 at K = 1024
+//   partials of 2 blocks: 6.9e-7 at K = 64, 3.2e-7 at K = 256, 1.9e-7 at K = 512
+//   partials of 1 block:  3.7e-7 at K = 64, 2.4e-7 at K = 128
+// while shorter partials cost speed (8192^3: 367, 355, 322, 204 TFLOP/s).  So
+// the length follows K, keeping every case near 4e-7 or below.
+int promote_blocks_for(int64_t k) {
+  if (k <= 128) return 1;
+  if (k <= 512) return 2;
+  if (k <= 2048) return 4;
+  return 8;
+}
+// Single TF32 (bound 2^-10) promotes every K = 1024.
+constexpr int kTf32PromoteBlocks = 32;
 // Tail split: at most this many K pieces per tile, each at least this many K blocks.
 constexpr int kMaxTailSplit = 8;
 constexpr int kMinPieceBlocks = 4;
@@ -61,6 +77,14 @@ struct Staging {
   Buffer a, b, c;
 };
 std::map<int, Staging> g_staging;
+// Copy streams and events of the host-buffer entry point, per device.
+constexpr int kMaxBands = 8;
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t ev[2 * kMaxBands + 2] = {};
+  bool ready = false;
+};
+std::map<int, HostPipe> g_pipes;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -325,10 +349,12 @@ phobos_status_t run_ffma(int64_t M, int64_t N, int64_t K, float alpha, const flo
   return st;
 }
 
+// reuse_b: the previous call on this stream split the same B (same N, K, ldb,
+// mode) into the workspace; skip that pre-pass unless the workspace moved.
 phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                        const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                        cudaStream_t stream, const phobos_gemm_plan_t &p, DeviceState &dev,
-                       int device) {
+                       int device, bool reuse_b = false) {
   const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
   const bool pair = p.cluster_m == 2;
   const int bm = pair ? 2 * kTcBM : kTcBM;
@@ -373,8 +399,10 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const size_t flag_bytes = static_cast<size_t>(round_up(slots * 2 * kEpiWarps * 4, 256));
   const size_t need = ops_bytes + part_bytes + flag_bytes;
   Buffer &ws = g_workspaces[{device, reinterpret_cast<uintptr_t>(stream)}];
+  void *const old_ws = ws.ptr;
   phobos_status_t st = ensure_buffer(ws, need, stream);
   if (st != PHOBOS_OK) return st;
+  if (ws.ptr != old_ws) reuse_b = false;
   float *partials = reinterpret_cast<float *>(static_cast<char *>(ws.ptr) + ops_bytes);
   unsigned *flags =
       reinterpret_cast<unsigned *>(static_cast<char *>(ws.ptr) + ops_bytes + part_bytes);
@@ -395,10 +423,12 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
                                                a_small, a_tma_ok, stream)));
     if (st != PHOBOS_OK) return st;
   }
-  st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
-                                             static_cast<int>(Np), static_cast<int>(Kp), b_big,
-                                             b_small, stream)));
-  if (st != PHOBOS_OK) return st;
+  if (!reuse_b) {
+    st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
+                                               static_cast<int>(Np), static_cast<int>(Kp), b_big,
+                                               b_small, stream)));
+    if (st != PHOBOS_OK) return st;
+  }
 
   TcArgs t{};
   // each CTA loads 128 rows of A and, in a pair, half of the tile's B rows
@@ -429,9 +459,9 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   if (gm > t.tiles_m) gm = t.tiles_m;
   t.group_m = static_cast<int>(gm);
   t.vec_c = (ldc % 4 == 0) && aligned16(C);
-  // Split TF32 needs short TMEM partial sums to stay at fp32 accuracy; single
-  // TF32 (a 2^-10 bound) promotes every K = 1024 only.
-  t.promote_blocks = passes == 3 ? kPromoteBlocks : 4 * kPromoteBlocks;
+  // Split TF32 needs short TMEM partial sums to stay at fp32 accuracy.
+  t.promote_blocks =
+      passes == 3 ? promote_blocks_for(p.super_k < K ? p.super_k : K) : kTf32PromoteBlocks;
   t.sm_count = dev.sm_count;
   t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD") ? 1 : 0;
   t.full_tiles = full_tiles;
@@ -493,7 +523,7 @@ phobos_status_t read_status_word(DeviceState &dev, cudaStream_t stream) {
 phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                            int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                            int64_t ldc, void *stream_ptr, phobos_math_t math,
-                           const phobos_gemm_plan_t *user_plan) {
+                           const phobos_gemm_plan_t *user_plan, bool reuse_b = false) {
   phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
   if (st != PHOBOS_OK) return st;
   if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
@@ -522,7 +552,8 @@ phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const f
   } else if (plan.path == PHOBOS_PATH_FFMA) {
     st = run_ffma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev);
   } else {
-    st = run_tc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev, device);
+    st = run_tc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev, device,
+                reuse_b);
   }
   if (st == PHOBOS_OK && env_flag("PHOBOS_DEBUG_SYNC")) st = read_status_word(*dev, stream);
   return st;
@@ -588,19 +619,86 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, 
     dB = static_cast<float *>(s.b.ptr);
     dC = static_cast<float *>(s.c.ptr);
   }
-  if (products) {
-    if (cudaMemcpyAsync(dA, A, a_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(dB, B, b_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+  // Large tensor-core problems run as row bands so that copies overlap the
+  // compute: B goes in first, then every band's rows of A (and C) on a copy
+  // stream; band i's GEMM runs on the caller's stream as soon as its rows are
+  // in (bands after the first reuse the first band's split of B), and its rows
+  // of C go back on a second copy stream while later bands compute.
+  phobos_gemm_plan_t plan;
+  if (products && (st = make_plan(M, N, K, math, &plan)) != PHOBOS_OK) return st;
+  int bands = 1;
+  if (products && plan.path != PHOBOS_PATH_FFMA && M >= 2048) {
+    bands = static_cast<int>(M / 1024);
+    if (bands > kMaxBands) bands = kMaxBands;
+  }
+  if (bands <= 1) {
+    if (products) {
+      if (cudaMemcpyAsync(dA, A, a_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+          cudaMemcpyAsync(dB, B, b_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return PHOBOS_ERR_CUDA;
+    }
+    if (beta != 0.0f &&
+        cudaMemcpyAsync(dC, C, c_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
+    st = sgemm_impl(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, stream_ptr, math, nullptr);
+    if (st != PHOBOS_OK) return st;
+    if (cudaMemcpyAsync(C, dC, c_elems * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+    return PHOBOS_OK;
+  }
+  HostPipe *pipe = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PHOBOS_ERR_CUDA;
+    pipe = &g_pipes[device];
+    if (!pipe->ready) {
+      if (cudaStreamCreateWithFlags(&pipe->in, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaStreamCreateWithFlags(&pipe->out, cudaStreamNonBlocking) != cudaSuccess)
+        return PHOBOS_ERR_CUDA;
+      for (cudaEvent_t &e : pipe->ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+          return PHOBOS_ERR_CUDA;
+      pipe->ready = true;
+    }
+  }
+  cudaEvent_t ev_start = pipe->ev[0], ev_end = pipe->ev[1];
+  cudaEvent_t *ev_in = pipe->ev + 2, *ev_done = pipe->ev + 2 + kMaxBands;
+  const int64_t rows = ((M + bands - 1) / bands + 255) / 256 * 256;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(ev_start, stream)) || !ok(cudaStreamWaitEvent(pipe->in, ev_start, 0)) ||
+      !ok(cudaStreamWaitEvent(pipe->out, ev_start, 0)) ||
+      !ok(cudaMemcpyAsync(dB, B, b_elems * 4, cudaMemcpyHostToDevice, pipe->in)))
+    return PHOBOS_ERR_CUDA;
+  int used = 0;
+  for (int64_t r0 = 0; r0 < M; r0 += rows, ++used) {
+    const int64_t r1 = r0 + rows < M ? r0 + rows : M;
+    const size_t a_off = static_cast<size_t>(r0 * lda), a_len = static_cast<size_t>((r1 - 1 - r0) * lda + K);
+    const size_t c_off = static_cast<size_t>(r0 * ldc), c_len = static_cast<size_t>((r1 - 1 - r0) * ldc + N);
+    if (!ok(cudaMemcpyAsync(dA + a_off, A + a_off, a_len * 4, cudaMemcpyHostToDevice, pipe->in)) ||
+        (beta != 0.0f &&
+         !ok(cudaMemcpyAsync(dC + c_off, C + c_off, c_len * 4, cudaMemcpyHostToDevice, pipe->in))) ||
+        !ok(cudaEventRecord(ev_in[used], pipe->in)))
       return PHOBOS_ERR_CUDA;
   }
-  if (beta != 0.0f &&
-      cudaMemcpyAsync(dC, C, c_elems * 4, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+  int band = 0;
+  for (int64_t r0 = 0; r0 < M; r0 += rows, ++band) {
+    const int64_t r1 = r0 + rows < M ? r0 + rows : M;
+    const size_t a_off = static_cast<size_t>(r0 * lda);
+    const size_t c_off = static_cast<size_t>(r0 * ldc), c_len = static_cast<size_t>((r1 - 1 - r0) * ldc + N);
+    if (!ok(cudaStreamWaitEvent(stream, ev_in[band], 0))) return PHOBOS_ERR_CUDA;
+    st = sgemm_impl(r1 - r0, N, K, alpha, dA + a_off, lda, dB, ldb, beta, dC + c_off, ldc,
+                    stream_ptr, math, nullptr, band > 0);
+    if (st != PHOBOS_OK) return st;
+    if (!ok(cudaEventRecord(ev_done[band], stream)) ||
+        !ok(cudaStreamWaitEvent(pipe->out, ev_done[band], 0)) ||
+        !ok(cudaMemcpyAsync(C + c_off, dC + c_off, c_len * 4, cudaMemcpyDeviceToHost, pipe->out)))
+      return PHOBOS_ERR_CUDA;
+  }
+  if (!ok(cudaEventRecord(ev_end, pipe->out)) || !ok(cudaStreamWaitEvent(stream, ev_end, 0)) ||
+      !ok(cudaStreamSynchronize(stream)))
     return PHOBOS_ERR_CUDA;
-  st = sgemm_impl(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc, stream_ptr, math, nullptr);
-  if (st != PHOBOS_OK) return st;
-  if (cudaMemcpyAsync(C, dC, c_elems * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return PHOBOS_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
   return PHOBOS_OK;
 }
 

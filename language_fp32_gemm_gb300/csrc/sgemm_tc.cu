@@ -22,7 +22,7 @@
 //    biases long sums (measured on GB300: at K = 8192 the split-TF32 error
 //    reached 3.7e-6 of sum|a||b| for random signs, and a -8.6e-5 mean bias for
 //    positive data).  So TMEM only holds a partial sum over `promote_blocks`
-//    K blocks (default 8, i.e. K = 256).  Two TMEM buffers alternate: while
+//    K blocks (1 to 8 for split TF32, shorter when K is short).  Two TMEM buffers alternate: while
 //    the MMAs fill one, eight epilogue warps read the other with tcgen05.ld and
 //    add it into fp32 registers with round-to-nearest adds.  This is the
 //    remedy of Ootomo & Yokota (2022) for tensor-core accumulation, done with

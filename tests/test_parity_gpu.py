@@ -286,3 +286,33 @@ def test_ffma_cluster_split_k(dev, shape, split):
     C1, _, _ = check(dev, A, B, C0, 0.5, -1.5, "ffma", plan=plan)
     C2 = run_gemm(torch, dev, A, B, C0, 0.5, -1.5, "ffma", plan=plan)
     assert np.array_equal(C1, C2)  # deterministic
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_host_buffer_entry_point_in_bands(dev, beta):
+    # M >= 2048 on the tensor-core path: row bands with overlapped copies;
+    # padded leading dimensions on every operand
+    M, N, K = 4100, 300, 200
+    A = padded(si.normal(96, 0, (M, K)), 3)
+    B = padded(si.normal(96, 1, (K, N)), 1)
+    C0 = si.uniform_pm1(96, 2, (M, N))
+    C = padded(C0, 2)  # a copy of C0 inside a wider buffer (ldc = N + 2)
+    lda, ldb, ldc = A.strides[0] // 4, B.strides[0] // 4, C.strides[0] // 4
+    st = phobos.phobos_sgemm_host(M, N, K, 1.5, A.ctypes.data, lda, B.ctypes.data, ldb, beta,
+                                  C.ctypes.data, ldc, 0, phobos.PHOBOS_MATH_3XTF32)
+    assert st == phobos.PHOBOS_OK
+    ref, den = oracle.sgemm(A, B, C0, 1.5, beta)
+    assert oracle.max_rel_error(C, ref, den) <= oracle.TOL_FP32
+
+
+# ----------------------------- split-TF32 accuracy where it is tightest
+
+@pytest.mark.parametrize("K", [32, 64, 128, 256, 512])
+def test_split_tf32_short_k_stress(dev, K):
+    # The tensor core truncates while it accumulates a TMEM partial sum; the
+    # error relative to sum|a||b| is largest when K spans few partials.  Two
+    # million normal-distributed outputs per K, all checked against the oracle.
+    M, N = 1024, 2048
+    A = si.normal(97, 0, (M, K))
+    B = si.normal(97, 1, (K, N))
+    check(dev, A, B, np.zeros((M, N), np.float32), 1.0, 0.0, "3xtf32")
