@@ -181,6 +181,19 @@ def oracle_rows_rate(w, A, B, C0, seconds):
         rows = min(w.M, int(math.ceil(rows * grow)))
 
 
+def aggregate_rate(local_ms, flops_per_rank, steps, world, device=None):
+    """Whole-job rate over `world` independent replicas: every rank processed
+    `steps` problems of `flops_per_rank`; the job's time is the slowest rank's.
+    Returns (max_ms, GFLOP/s).  Collective only when world > 1."""
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    return max_ms, world * flops_per_rank * steps / (max_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -314,12 +327,8 @@ def run_phobos(args):
 
     elapsed_ms = t_start.elapsed_time(t_stop)
     kernel_ms = [a.elapsed_time(b) for a, b in kev]
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
     flops = 2.0 * M * N * K
-    value = world * flops * args.steps / (max_ms / 1e3) / 1e9
+    max_ms, value = aggregate_rate(elapsed_ms, flops, args.steps, world, dev)
 
     # ------------------------------------------------ end to end, host buffers
     C_out = torch.empty_like(C_p).pin_memory()
@@ -340,10 +349,7 @@ def run_phobos(args):
             e2e_ms.append(e0.elapsed_time(e1))
     h2d = 4 * (M * K + K * N + (M * N if w.beta != 0 else 0))
     d2h = 4 * M * N
-    e2e_t = torch.tensor([sum(e2e_ms) / len(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = world * flops / (float(e2e_t.item()) / 1e3) / 1e9
+    _, e2e_value = aggregate_rate(sum(e2e_ms) / len(e2e_ms), flops, 1, world, dev)
 
     if world > 1:
         dist.barrier()
@@ -385,7 +391,10 @@ def run_phobos(args):
         "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        # arithmetic of the path: tf32 products with fp32 accumulation (x3 for
+        # the split), or fp32 fused multiply-add
+        "dtype": {"3xtf32": "3xtf32", "tf32": "tf32", "ffma": "f32"}[path_name],
+        "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "alpha": w.alpha,
                    "beta": w.beta, "seed": w.seed, "math": path_name,
                    "plan": plan.as_dict(), "parallelism": "replicas" if world > 1 else "single",

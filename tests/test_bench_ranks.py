@@ -1,0 +1,54 @@
+"""bench.py's multi-rank path on CPU: two gloo ranks, each an independent
+replica, aggregate to the slowest rank's time and the whole job's rate."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local_ms = [120.0, 150.0][rank]   # rank 1 is the slower replica
+    max_ms, gflops = bench.aggregate_rate(local_ms, 2.0e9, 10, world)
+    out[rank] = (max_ms, gflops)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_with_gloo():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    # both ranks see the slowest rank's time; the rate counts both replicas
+    for r in range(2):
+        max_ms, gflops = out[r]
+        assert max_ms == 150.0
+        assert gflops == pytest.approx(2 * 2.0e9 * 10 / 0.150 / 1e9)
+
+
+def test_single_rank_needs_no_collective():
+    sys.path.insert(0, ROOT)
+    import bench
+    max_ms, gflops = bench.aggregate_rate(50.0, 1.0e9, 4, 1)
+    assert max_ms == 50.0 and gflops == pytest.approx(4 * 1.0e9 / 0.05 / 1e9)
