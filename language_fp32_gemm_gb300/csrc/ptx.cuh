@@ -335,6 +335,27 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       : "memory");
 }
 
+// ------------------------------------------------- per-thread async copies
+// Global -> shared copies that complete in the background (LDGSTS); a thread
+// waits for its own copies with cp_async_wait_all, then a warp or CTA barrier
+// makes them visible to the other threads.
+__device__ __forceinline__ void cp_async4(float *smem_dst, const float *gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
+               "l"(__cvta_generic_to_global(gmem_src))
+               : "memory");
+}
+
+// 16-byte copy: both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(float *smem_dst, const float *gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(__cvta_generic_to_global(gmem_src))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------- global flags between CTAs
 
 __device__ __forceinline__ void st_release_gpu(unsigned *addr, unsigned v) {

@@ -483,9 +483,43 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     int c_glob = 0;
     bool ok = true;
     Unit u;
+    constexpr int kRanks = PAIR ? 2 : 1;
+    float *sbuf = epi_stage + (warp - 2) * 32 * 32;  // this warp's 32 x 32 block of C
     for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
       int tm, tn;
       raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      // This warp owns rows row0 .. row0+31 and columns col0 .. col0+kHalf-1 of
+      // the tile; lane l sums row row0 + l.
+      const int tile_row = static_cast<int>(rank) * kBM + q * 32 + lane;  // 0 .. kTileM-1
+      const int row0 = tm * kTileM + tile_row - lane;
+      const int col0 = tn * BN + h * kHalf;
+      const bool writes_c = u.piece <= 0 && row0 < p.M && col0 < p.N;  // warp-uniform
+      const bool vec = p.vec_c && col0 + kHalf <= p.N;                  // 16-byte rows
+      const bool load_old = writes_c && p.beta != 0.0f;
+      // Old C of columns j0 .. j0+31 into the warp's block, in the swizzled
+      // layout the row-per-lane reads below use: row r, column c at
+      // r*32 + (c ^ r) (4-byte copies), or 16-byte chunk ch at chunk ch ^ (r & 7).
+      // Each copy instruction covers whole 128-byte row segments.
+      auto fetch_old = [&](int j0) {
+        if (vec) {
+#pragma unroll 4
+          for (int k = 0; k < 8; ++k) {
+            const int r = 4 * k + (lane >> 3), ch = lane & 7;
+            if (row0 + r < p.M)
+              cp_async16(sbuf + r * 32 + ((ch ^ (r & 7)) << 2),
+                         p.C + static_cast<int64_t>(row0 + r) * p.ldc + col0 + j0 + 4 * ch);
+          }
+        } else {
+          const int col = col0 + j0 + lane;
+          if (col < p.N) {
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r)
+              if (row0 + r < p.M)
+                cp_async4(sbuf + r * 32 + (lane ^ r), p.C + static_cast<int64_t>(row0 + r) * p.ldc + col);
+          }
+        }
+      };
+      bool first_fetched = false;
       float sum[kHalf];
 #pragma unroll
       for (int j = 0; j < kHalf; ++j) sum[j] = 0.f;
@@ -493,6 +527,12 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       for (int c = 0; c < n_chunks; ++c, ++c_glob) {
         const int b = c_glob & 1;
         const uint32_t use = static_cast<uint32_t>(c_glob >> 1);
+        if (c == n_chunks - 1 && load_old) {
+          // The first block of old C does not depend on the sums: fetch it
+          // while the tile's last partial sum is still being accumulated.
+          fetch_old(0);
+          first_fetched = true;
+        }
         if (!bounded_wait(acc_full0 + 8u * b, use & 1u, abort_flag, p.err, kDevTimeoutEpilogue)) {
           ok = false;
           abort_peer();
@@ -517,19 +557,23 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             mbar_arrive(acc_empty0 + 8u * b);
         }
       }
-      if (!ok) break;
-      // Tail pieces: this thread's 1 x kHalf slice of the tile in slot order.
-      const int tile_row = static_cast<int>(rank) * kBM + q * 32 + lane;  // 0 .. kTileM-1
+      if (!ok) {
+        cp_async_wait_all();  // no copy may land in a buffer after the CTA exits
+        break;
+      }
+      // Tail pieces exchange their partial sums through L2 in a warp-interleaved
+      // layout: float4 v of lane l of a warp sits at (v * 32 + l), so that every
+      // store and load instruction covers 512 contiguous bytes.
       if (u.piece > 0) {
-        // Hand the partial sum to the piece-0 owner through L2, then release
-        // the flag once every accumulator thread's stores are visible.
+        // Hand the partial sum to the piece-0 owner, then release the flag once
+        // every accumulator thread's stores are visible.
         const long long slot = static_cast<long long>(u.tile - p.full_tiles) * (p.tail_split - 1) +
                                (u.piece - 1);
-        float4 *dst = reinterpret_cast<float4 *>(
-            p.partials + (slot * kTileM + tile_row) * BN + h * kHalf);
+        float4 *dst = reinterpret_cast<float4 *>(p.partials) +
+                      ((slot * kRanks + rank) * kEpiWarps + (warp - 2)) * (kHalf / 4) * 32 + lane;
 #pragma unroll
         for (int v = 0; v < kHalf / 4; ++v)
-          __stcg(dst + v, make_float4(sum[4 * v], sum[4 * v + 1], sum[4 * v + 2], sum[4 * v + 3]));
+          __stcg(dst + v * 32, make_float4(sum[4 * v], sum[4 * v + 1], sum[4 * v + 2], sum[4 * v + 3]));
         // Each warp publishes its own slice: no CTA-wide barrier, so a warp
         // that left on an abort path cannot strand the others.
         __threadfence();
@@ -558,89 +602,83 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             }
           }
           if (!ok) break;
-          const float4 *src = reinterpret_cast<const float4 *>(
-              p.partials + (slot * kTileM + tile_row) * BN + h * kHalf);
+          const float4 *src = reinterpret_cast<const float4 *>(p.partials) +
+                              ((slot * kRanks + rank) * kEpiWarps + (warp - 2)) * (kHalf / 4) * 32 +
+                              lane;
 #pragma unroll
           for (int v = 0; v < kHalf / 4; ++v) {
-            const float4 x = __ldcg(src + v);
+            const float4 x = __ldcg(src + v * 32);
             sum[4 * v + 0] = __fadd_rn(sum[4 * v + 0], x.x);
             sum[4 * v + 1] = __fadd_rn(sum[4 * v + 1], x.y);
             sum[4 * v + 2] = __fadd_rn(sum[4 * v + 2], x.z);
             sum[4 * v + 3] = __fadd_rn(sum[4 * v + 3], x.w);
           }
         }
-        if (!ok) break;
+        if (!ok) {
+          cp_async_wait_all();
+          break;
+        }
       }
+      if (!writes_c) continue;
       // The tile's sum is in registers: TMEM already serves the next tile's
-      // MMAs while this store runs.  The old C values of a block are all
-      // loaded before any store, so the loads overlap instead of waiting on
-      // one another.
-      const int row = tm * kTileM + tile_row;
-      const int col0 = tn * BN + h * kHalf;
+      // MMAs while this store runs.  Per 32-column block: old C lands in the
+      // warp's block (asynchronous copies), each lane combines its row in
+      // place, then the warp writes the block back row by row.
       const float alpha = p.alpha, beta = p.beta;
-      if (p.vec_c && col0 + kHalf <= p.N) {  // warp-uniform
-        // Aligned C: each thread writes its row segment with 16-byte stores.
-        if (row < p.M) {
-          float4 *dst = reinterpret_cast<float4 *>(p.C + static_cast<int64_t>(row) * p.ldc + col0);
 #pragma unroll
-          for (int v0 = 0; v0 < kHalf / 4; v0 += 4) {
-            float4 old[4];
-            if (beta != 0.0f) {
+      for (int j0 = 0; j0 < kHalf; j0 += 32) {
+        if (col0 + j0 >= p.N) break;  // uniform across the warp
+        if (load_old) {
+          if (j0 > 0 || !first_fetched) fetch_old(j0);
+          cp_async_wait_all();
+          __syncwarp();
+        }
+        if (vec) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) old[i] = dst[v0 + i];
+          for (int jj = 0; jj < 8; ++jj) {
+            float4 *s4 = reinterpret_cast<float4 *>(sbuf + lane * 32 + ((jj ^ (lane & 7)) << 2));
+            float4 o;
+            if (load_old) {
+              const float4 old = *s4;
+              o.x = fmaf(alpha, sum[j0 + 4 * jj + 0], beta * old.x);
+              o.y = fmaf(alpha, sum[j0 + 4 * jj + 1], beta * old.y);
+              o.z = fmaf(alpha, sum[j0 + 4 * jj + 2], beta * old.z);
+              o.w = fmaf(alpha, sum[j0 + 4 * jj + 3], beta * old.w);
+            } else {
+              o.x = alpha * sum[j0 + 4 * jj + 0];
+              o.y = alpha * sum[j0 + 4 * jj + 1];
+              o.z = alpha * sum[j0 + 4 * jj + 2];
+              o.w = alpha * sum[j0 + 4 * jj + 3];
             }
+            *s4 = o;
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int v = v0 + i;
-              float4 o;
-              if (beta != 0.0f) {
-                o.x = fmaf(alpha, sum[4 * v + 0], beta * old[i].x);
-                o.y = fmaf(alpha, sum[4 * v + 1], beta * old[i].y);
-                o.z = fmaf(alpha, sum[4 * v + 2], beta * old[i].z);
-                o.w = fmaf(alpha, sum[4 * v + 3], beta * old[i].w);
-              } else {
-                o.x = alpha * sum[4 * v + 0];
-                o.y = alpha * sum[4 * v + 1];
-                o.z = alpha * sum[4 * v + 2];
-                o.w = alpha * sum[4 * v + 3];
-              }
-              dst[v] = o;
-            }
+          for (int j = 0; j < 32; ++j) {
+            float &s = sbuf[lane * 32 + (j ^ lane)];
+            s = load_old ? fmaf(alpha, sum[j0 + j], beta * s) : alpha * sum[j0 + j];
           }
         }
-      } else {
-        // Any ldc, alignment or edge: the warp transposes 32 x 32 blocks through
-        // shared memory (XOR-swizzled, conflict-free), so each load and store
-        // instruction covers 32 consecutive columns of one row.
-        const int row0 = row - lane;
-        float *sbuf = epi_stage + (warp - 2) * 32 * 32;
-#pragma unroll
-        for (int j0 = 0; j0 < kHalf; j0 += 32) {
+        __syncwarp();
+        if (vec) {
+#pragma unroll 4
+          for (int k = 0; k < 8; ++k) {
+            const int r = 4 * k + (lane >> 3), ch = lane & 7;
+            if (row0 + r < p.M)
+              *reinterpret_cast<float4 *>(p.C + static_cast<int64_t>(row0 + r) * p.ldc + col0 + j0 +
+                                          4 * ch) =
+                  *reinterpret_cast<const float4 *>(sbuf + r * 32 + ((ch ^ (r & 7)) << 2));
+          }
+        } else {
           const int col = col0 + j0 + lane;
-          if (col0 + j0 >= p.N) break;  // uniform across the warp
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sbuf[lane * 32 + (j ^ lane)] = sum[j0 + j];
-          __syncwarp();
-#pragma unroll 1
-          for (int r0 = 0; r0 < 32; r0 += 8) {
-            float old[8];
-            if (beta != 0.0f) {
-#pragma unroll
-              for (int r = 0; r < 8; ++r)
-                old[r] = (row0 + r0 + r < p.M && col < p.N)
-                             ? p.C[static_cast<int64_t>(row0 + r0 + r) * p.ldc + col]
-                             : 0.0f;
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              const float v = sbuf[(r0 + r) * 32 + (lane ^ (r0 + r))];
-              if (row0 + r0 + r < p.M && col < p.N)
-                p.C[static_cast<int64_t>(row0 + r0 + r) * p.ldc + col] =
-                    beta != 0.0f ? fmaf(alpha, v, beta * old[r]) : alpha * v;
-            }
+          if (col < p.N) {
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r)
+              if (row0 + r < p.M)
+                p.C[static_cast<int64_t>(row0 + r) * p.ldc + col] = sbuf[r * 32 + (lane ^ r)];
           }
-          __syncwarp();
         }
+        __syncwarp();
       }
     }
   }
