@@ -93,10 +93,18 @@ def kernel_traffic(kernel_file, workload, math_name):
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if not m_sha or not m_tr:
         return None
-    src = open(os.path.join(ROOT, "language_fp32_gemm_gb300", "csrc", kernel_file), "rb").read()
-    if hashlib.sha256(src).hexdigest() != m_sha.group(1):
+    if kernel_source_sha256(kernel_file) != m_sha.group(1):
         return None
     return int(m_tr.group(1))
+
+
+def kernel_source_sha256(kernel_file):
+    """SHA-256 over the kernel's source and the two headers it is built from."""
+    h = hashlib.sha256()
+    for name in (kernel_file, "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "language_fp32_gemm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:
