@@ -15,8 +15,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libphobos_gemm.so")
-SOURCES = ["phobos_gemm.cu", "sgemm_tc.cu", "sgemm_ffma.cu", "split.cu", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "internal.h", os.path.join("..", "..", "include", "phobos_gemm.h")]
+SOURCES = ["phobos_gemm.cu", "sgemm_tc.cu", "sgemm_ffma.cu", "split.cu", "noalloc.cu",
+           "cluster_plan.cc", "cluster_pod.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "cluster_internal.h",
+           os.path.join("..", "..", "include", "phobos_gemm.h"),
+           os.path.join("..", "..", "include", "phobos_cluster.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -44,7 +47,7 @@ def build(force=False, verbose=False, extra_flags=()):
     objects, jobs = [], []
     for src in SOURCES:
         src_path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objects.append(obj)
         if force or _stale(obj, [src_path] + headers):
             cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src_path, "-o", obj]

@@ -11,6 +11,7 @@ from language_fp32_gemm_gb300 import build as lib_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "phobos_gemm.h")
+CLUSTER_HEADER = os.path.join(ROOT, "include", "phobos_cluster.h")
 
 
 @pytest.fixture(scope="module")
@@ -19,9 +20,10 @@ def lib():
     return phobos.library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"\(\*\w+\)\s*\(", "(", text)  # function-pointer members are not exports
     return sorted(set(re.findall(r"\b(phobos_\w+)\s*\(", text)))
 
 
@@ -30,11 +32,17 @@ def test_header_declares_the_abi():
     assert set(names) == set(phobos.ABI_FUNCTIONS), names
 
 
+def test_cluster_header_declares_the_cluster_abi():
+    from language_fp32_gemm_gb300 import cluster
+    names = declared_functions(CLUSTER_HEADER)
+    assert set(names) == set(cluster.CLUSTER_ABI_FUNCTIONS), names
+
+
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", phobos.LIBRARY_PATH],
                          capture_output=True, text=True, check=True).stdout
     exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
-    for name in declared_functions():
+    for name in declared_functions() + declared_functions(CLUSTER_HEADER):
         assert name in exported, name
         assert getattr(lib, name) is not None
 
