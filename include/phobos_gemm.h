@@ -99,7 +99,7 @@ typedef enum {
  *                  many, capped so every piece spans at least K = 128).
  *                  Results are equal up to rounding order and deterministic.
  *  a_split         tensor-core paths: where A is split into tf32 big/small
- *                  (0 = chosen per call: inside the kernel when N <= 512 and
+ *                  (0 = chosen per call: inside the kernel when N <= 1536 and
  *                  A's rows are 16-byte aligned, where a separate pass over A
  *                  would cost a large share of the GEMM; 1 = a pre-pass into
  *                  the workspace; 2 = inside the kernel, which needs

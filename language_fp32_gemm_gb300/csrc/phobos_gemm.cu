@@ -51,9 +51,10 @@ constexpr int kMinPieceBlocks = 4;
 constexpr int kEpiWarps = 8;  // accumulator warps of the tensor-core kernel (one flag each)
 // Automatic a_split: split A inside the kernel up to this N.  A pre-pass over
 // A costs about 6 * (TF32/3 rate) / (N * HBM bandwidth) of the GEMM time,
-// ~300/N on GB300; splitting inside the kernel slows the main loop by ~50 %
-// (two converter warps), measured on GB300.  They cross near N = 600.
-constexpr int64_t kInlineSplitMaxN = 512;
+// ~300/N on GB300; splitting inside the kernel slows the main loop by about
+// 15-20 % (the converter warps' share of the SM), measured on GB300 at
+// M = 16384, K = 4096.  They cross between N = 1536 and N = 2048.
+constexpr int64_t kInlineSplitMaxN = 1536;
 
 std::mutex g_mutex;       // planner caches, device state, workspaces
 std::mutex g_host_mutex;  // serialises the host-buffer entry point (shared staging)

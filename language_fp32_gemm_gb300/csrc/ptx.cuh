@@ -105,6 +105,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
       : "memory");
 }
 
+// Bring one box of a tensor map into L2 (no shared memory, no barrier); the
+// x coordinate follows the same 16-byte rule as a load.
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 // Warp-wide: allocate `ncols` TMEM columns (power of two >= 32); the base

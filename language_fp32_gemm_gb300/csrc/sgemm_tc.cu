@@ -72,6 +72,13 @@ constexpr int kCvtWarps = 2;  // warps 10, 11: split A in shared memory (in-kern
 constexpr int threads_for(bool asplit) { return kThreads + (asplit ? 32 * kCvtWarps : 0); }
 constexpr int kSmemLimit = 227 * 1024;
 constexpr uint64_t kAbortGraceNs = 200000;  // let copies in flight land before exit
+// With A split inside the kernel, the producer asks L2 for the caller's raw A
+// this many k blocks ahead of its loads. Each raw A tile is read once, from
+// HBM, and its stage then waits for the split and the pair's relay, so the
+// load itself has little slack. Measured on GB300: 2 to 8 blocks ahead give
+// the same gain (about 10 % at 65536x256x4096). Prefetching the pre-split
+// operands of the other path, which are re-read from L2, made it slower.
+constexpr int kRawAPrefetchAhead = 2;
 
 template <int BN, int PASSES, bool PAIR>
 struct TcShape {
@@ -133,6 +140,36 @@ __device__ __forceinline__ bool unit_of(const TcArgs &p, int w, int units, int i
   return true;
 }
 
+// Walks the same (unit, k block) sequence as the loads of the caller's raw A,
+// ahead of them, and prefetches each k block's A box into L2.
+template <bool PAIR>
+struct RawAPrefetch {
+  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;
+  int i = 0, kb = 0, m0 = 0;
+  bool valid = false;
+  Unit u;
+
+  __device__ __forceinline__ void start(const TcArgs &p, int w, int units, uint32_t rank) {
+    valid = unit_of(p, w, units, 0, u);
+    if (valid) enter(p, rank);
+  }
+  __device__ __forceinline__ void enter(const TcArgs &p, uint32_t rank) {
+    int tm, tn;
+    raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    m0 = tm * kTileM + static_cast<int>(rank) * kBM;
+    kb = u.k_lo;
+  }
+  // Prefetch the current k block's box (when it starts inside A), then step.
+  __device__ __forceinline__ void step(const TcArgs &p, int w, int units, uint32_t rank) {
+    if (!valid) return;
+    if (m0 < p.M) tma_prefetch_2d(&p.tmap_ab, (p.k_block0 + kb) * kBK, m0);
+    if (++kb >= u.k_hi) {
+      valid = unit_of(p, w, units, ++i, u);
+      if (valid) enter(p, rank);
+    }
+  }
+};
+
 template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT>
 __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
@@ -187,7 +224,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     if (ASPLIT) {
       for (int s = 0; s < STAGES; ++s) {
         mbar_init(a_full0 + 8u * s, 1);
-        mbar_init(conv0 + 8u * s, (PAIR ? 2 : 1) * kCvtWarps);
+        // this CTA's converter warps, plus the peer's relay on the leader
+        mbar_init(conv0 + 8u * s, kCvtWarps + (PAIR && leader ? 1 : 0));
       }
     }
     *abort_flag = 0;
@@ -243,26 +281,33 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         float4 *big = reinterpret_cast<float4 *>(smem_raw + (tiles - raw) + s * S::kStageBytes) +
                       cw * kPerWarp;
         float4 *small = big + S::kATile / 16;
-#pragma unroll 8
-        for (int j = 0; j < kPerWarp / 32; ++j) {
-          const int idx = j * 32 + lane;
-          const float4 x = big[idx];
-          float4 b, sm;
-          b.x = tf32_rna_bits(x.x); sm.x = tf32_rna_bits(x.x - b.x);
-          b.y = tf32_rna_bits(x.y); sm.y = tf32_rna_bits(x.y - b.y);
-          b.z = tf32_rna_bits(x.z); sm.z = tf32_rna_bits(x.z - b.z);
-          b.w = tf32_rna_bits(x.w); sm.w = tf32_rna_bits(x.w - b.w);
-          big[idx] = b;
-          if (PASSES == 3) small[idx] = sm;
+        // Batches of 8 vectors: all loads first, so they overlap (the stores
+        // of one vector could otherwise hold back the next vector's load).
+        constexpr int kBatch = 8;
+        static_assert((kPerWarp / 32) % kBatch == 0, "whole batches per warp");
+#pragma unroll 1
+        for (int j0 = 0; j0 < kPerWarp / 32; j0 += kBatch) {
+          float4 x[kBatch];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) x[j] = big[(j0 + j) * 32 + lane];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            float4 b, sm;
+            b.x = tf32_rna_bits(x[j].x); sm.x = tf32_rna_bits(x[j].x - b.x);
+            b.y = tf32_rna_bits(x[j].y); sm.y = tf32_rna_bits(x[j].y - b.y);
+            b.z = tf32_rna_bits(x[j].z); sm.z = tf32_rna_bits(x[j].z - b.z);
+            b.w = tf32_rna_bits(x[j].w); sm.w = tf32_rna_bits(x[j].w - b.w);
+            big[(j0 + j) * 32 + lane] = b;
+            if (PASSES == 3) small[(j0 + j) * 32 + lane] = sm;
+          }
         }
         fence_proxy_async_shared();  // the tensor core reads these through the async proxy
         __syncwarp();
-        if (lane == 0) {
-          if (PAIR)
-            mbar_arrive_cluster(mapa_shared(conv0 + 8u * s, 0));
-          else
-            mbar_arrive(conv0 + 8u * s);
-        }
+        // A CTA-scope arrive on this CTA's own barrier. In the peer, the relay
+        // thread forwards it to the leader; a cluster-scope release arrive here
+        // would cost the converters about 1300 cycles per stage (measured),
+        // more than the stage's MMAs.
+        if (lane == 0) mbar_arrive(conv0 + 8u * s);
       }
     }
   } else if (warp == 0 && ASPLIT) {
@@ -272,6 +317,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       int g = 0;
       bool ok = true;
       Unit u;
+      RawAPrefetch<PAIR> pf;
+      pf.start(p, unit, units, rank);
+      for (int j = 0; j < kRawAPrefetchAhead; ++j) pf.step(p, unit, units, rank);
       for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
         int tm, tn;
         raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
@@ -303,6 +351,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             tma_load_2d(bt, &p.tmap_bb, full, kc, b_row);
             if (PASSES == 3) tma_load_2d(bt + S::kBTile, &p.tmap_bs, full, kc, b_row);
           }
+          // after this stage's loads, so they never queue behind a prefetch
+          pf.step(p, unit, units, rank);
           armed |= 1u << s;
           last_parity = (last_parity & ~(1u << s)) | (ph << s);
         }
@@ -474,6 +524,28 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       else
         mma_commit(mma_drained);
       bounded_wait(mma_drained, 0, abort_flag, p.err, kDevTimeoutDrain, false);
+    } else if (ASPLIT && PAIR && lane == 0) {
+      // Relay, in the peer, whose MMA warp issues nothing: once this CTA's
+      // converter warps have split a stage, tell the leader's MMA issuer. The
+      // release at cluster scope carries the converters' shared-memory writes
+      // (ordered before it by their arrive and this thread's wait) to the
+      // leader, which acquires them before its MMAs read this CTA's A.
+      int g = 0;
+      bool ok = true;
+      Unit u;
+      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+        for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1u;
+          if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+          if (!bounded_wait(conv0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutProducer)) {
+            abort_peer();
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(mapa_shared(conv0 + 8u * s, 0));
+        }
+      }
     }
   } else {
     // ------------------------------------------- accumulate + epilogue warps
