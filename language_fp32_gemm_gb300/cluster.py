@@ -510,7 +510,12 @@ class Scheduler:
             gen[n] = g
             self.store.set("gen/%d" % n, str(g))
 
-    def run(self, poll=0.02, deadline=3600.0):
+    def run(self, poll=0.02, deadline=3600.0, alive=None):
+        """Plan, deal, watch and re-plan until every output is stored.
+
+        ``alive`` (optional) returns False once no pod process is left, so
+        that registration fails at once instead of at its timeout.
+        """
         job = self.job
         self.store.set("job", job_text(job))
         self.store.set("budget", str(self.budget))
@@ -520,6 +525,8 @@ class Scheduler:
         while time.time() - t_reg < self.register_timeout:
             if self.store.check(["hb/%d" % n for n in range(self.nodes)]):
                 break
+            if alive is not None and not alive():
+                raise RuntimeError("every pod process exited before registering")
             time.sleep(poll)
         self.live = [n for n in range(self.nodes) if self.store.check(["hb/%d" % n])]
         if not self.live:
@@ -600,6 +607,8 @@ def run_local(job, nodes, budget, device=DEVICE_CUDA, autotune=False, heartbeat=
     """Run `job` on `nodes` pod processes of this machine, with the scheduler here.
 
     ``fail`` maps a node to the ``exit_at`` of its pod (see :func:`pod_main`).
+    Pods are started with the "spawn" method, so a script that calls this
+    must do so under ``if __name__ == "__main__":``.
     ``host_gemm`` (picklable; host device only) computes the leaves of the
     host-memory pods used by the host-logic tests. Returns the finished
     :class:`Scheduler` (``super``, ``replans``, ``log``, ``elapsed``).
@@ -622,7 +631,7 @@ def run_local(job, nodes, budget, device=DEVICE_CUDA, autotune=False, heartbeat=
         pr.start()
         procs.append(pr)
     try:
-        sched.run(deadline=deadline)
+        sched.run(deadline=deadline, alive=lambda: any(pr.is_alive() for pr in procs))
     finally:
         for pr in procs:
             pr.join(timeout=30)
