@@ -27,7 +27,8 @@ namespace {
 constexpr int kBK = 8;
 
 template <int BM, int BN, bool KSPLIT>
-__global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const FfmaArgs p) {
+__global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 1)
+    sgemm_ffma_kernel(const FfmaArgs p) {
   constexpr int NT = (BM / 8) * (BN / 8);
   constexpr int PAD = 4;
   constexpr int A_LOADS = BM * kBK / 4 / NT;  // float4 groups of A per thread
@@ -121,15 +122,25 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8)) sgemm_ffma_kernel(const F
   load_tiles(k_lo);
   store_tiles(0);
   __syncthreads();
+  // The fragments of step k + 1 are read from shared memory while step k's
+  // FMAs run, so the FMAs do not wait on the shared-memory latency (which
+  // was the kernel's main stall).
+  float4 fa[2][2], fb[2][2];
+  auto load_frag = [&](int b, int k, int slot) {
+    fa[slot][0] = *reinterpret_cast<const float4 *>(&As[b][k][ty * 4]);
+    fa[slot][1] = *reinterpret_cast<const float4 *>(&As[b][k][ty * 4 + BM / 2]);
+    fb[slot][0] = *reinterpret_cast<const float4 *>(&Bs[b][k][tx * 4]);
+    fb[slot][1] = *reinterpret_cast<const float4 *>(&Bs[b][k][tx * 4 + BN / 2]);
+  };
   for (int k0 = k_lo; k0 < k_end; k0 += kBK) {
     const bool more = k0 + kBK < k_end;
     if (more) load_tiles(k0 + kBK);  // global loads in flight during the FMAs
+    load_frag(buf, 0, 0);
 #pragma unroll
     for (int k = 0; k < kBK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][ty * 4 + BM / 2]);
-      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][tx * 4 + BN / 2]);
+      if (k + 1 < kBK) load_frag(buf, k + 1, (k + 1) & 1);
+      const float4 a0 = fa[k & 1][0], a1 = fa[k & 1][1];
+      const float4 b0 = fb[k & 1][0], b1 = fb[k & 1][1];
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
