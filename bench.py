@@ -42,7 +42,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["phobos", "reference"], default="phobos")
     ap.add_argument("--workload", default="sgemm_8192")
-    ap.add_argument("--math", default="default", choices=["default", "3xtf32", "tf32", "ffma"])
+    ap.add_argument("--math", default="default",
+                    choices=["default", "3xtf32", "tf32", "ffma", "fp16", "bf16"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target host time of the oracle baseline sample")
@@ -72,6 +73,9 @@ def load_peaks():
 
 def peak_for(path_name, peaks):
     """Roofline denominator of the main kernel, by path."""
+    if path_name in ("fp16", "bf16"):
+        # 16-bit inputs run at the dense bf16/fp16 rate: the measured bf16 peak itself
+        return ("tensor", peaks["bf16_tflops"], "TFLOP/s", "bf16 burst (fp16 has the same dense rate)")
     if path_name in ("3xtf32", "tf32"):
         tf32 = peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
         return ("tensor", tf32 / 3.0 if path_name == "3xtf32" else tf32, "TFLOP/s",
@@ -280,7 +284,8 @@ def run_phobos(args):
     dC = dC0.clone()
     plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, args.math)
     path_name = {phobos.PHOBOS_PATH_FFMA: "ffma", phobos.PHOBOS_PATH_TF32: "tf32",
-                 phobos.PHOBOS_PATH_3XTF32: "3xtf32"}[plan.path]
+                 phobos.PHOBOS_PATH_3XTF32: "3xtf32", phobos.PHOBOS_PATH_FP16: "fp16",
+                 phobos.PHOBOS_PATH_BF16: "bf16"}[plan.path]
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -373,11 +378,12 @@ def run_phobos(args):
     achieved = flops / (avg_kernel_ms / 1e3) / 1e12
     clk = clocks.summary(wall0, wall1) if clocks else None
     # Per-clock view: nominal dense tensor rate per SM (tf32: 4096 flop/clk/SM,
-    # i.e. 1.1 PFLOP/s at ~1.77 GHz) at the SM clock sampled during the run.
+    # i.e. 1.1 PFLOP/s at ~1.77 GHz; fp16/bf16: 8192) at the SM clock sampled
+    # during the run.
     per_clock = None
     if bound == "tensor" and clk and clk.get("sm_mhz"):
         tf32_clk = SMS * 4096 * clk["sm_mhz"] * 1e6 / 1e12
-        per_clock = tf32_clk / 3.0 if path_name == "3xtf32" else tf32_clk
+        per_clock = {"3xtf32": tf32_clk / 3.0, "tf32": tf32_clk}.get(path_name, 2 * tf32_clk)
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_file, args.workload,
                                                                     path_name),
@@ -400,8 +406,10 @@ def run_phobos(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         # arithmetic of the path: tf32 products with fp32 accumulation (x3 for
-        # the split), or fp32 fused multiply-add
-        "dtype": {"3xtf32": "3xtf32", "tf32": "tf32", "ffma": "f32"}[path_name],
+        # the split), fp16 / bf16 products with fp32 accumulation, or fp32
+        # fused multiply-add
+        "dtype": {"3xtf32": "3xtf32", "tf32": "tf32", "ffma": "f32", "fp16": "f16",
+                  "bf16": "bf16"}[path_name],
         "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "alpha": w.alpha,
                    "beta": w.beta, "seed": w.seed, "math": path_name,

@@ -59,25 +59,43 @@ typedef enum {
 } phobos_status_t;
 
 /* How the products are formed.  DEFAULT picks FFMA for small problems and
- * split TF32 (3xTF32) on the tensor cores otherwise. */
+ * split TF32 (3xTF32) on the tensor cores otherwise.
+ *
+ * FP16 and BF16 are the reduced-precision tensor-core mode of "Show HN:
+ * Phobos", section "Side-quest: Cheating": the fp32 inputs are cast to a
+ * 16-bit type before the tensor cores, the products are accumulated in fp32,
+ * and the result is fp32.  Here the pre-pass rounds A and B to nearest
+ * (ties to even).  Each product of two 16-bit values is exact in fp32.  The
+ * result is therefore alpha * sum(r(a) * r(b)) + beta * C up to the fp32
+ * accumulation, with r() the rounding (relative error <= 2^-11 for fp16,
+ * 2^-8 for bf16).  This is not the fp32 accuracy of the other modes: it is
+ * the mode the pages call apples to oranges.  fp16 keeps 5 exponent bits:
+ * inputs beyond +-65504 become infinities, and tiny inputs lose precision.
+ * bf16 keeps fp32's exponent range. */
 typedef enum {
   PHOBOS_MATH_DEFAULT = 0,
   PHOBOS_MATH_3XTF32 = 1, /* a = a_big + a_small, three tf32 products, fp32-level accuracy */
   PHOBOS_MATH_TF32 = 2,   /* one tf32 product per term (10-bit mantissa operands) */
-  PHOBOS_MATH_FFMA = 3    /* fp32 fused multiply-add on the CUDA cores */
+  PHOBOS_MATH_FFMA = 3,   /* fp32 fused multiply-add on the CUDA cores */
+  PHOBOS_MATH_FP16 = 4,   /* inputs rounded to fp16, fp32 accumulation on the tensor cores */
+  PHOBOS_MATH_BF16 = 5    /* inputs rounded to bf16, fp32 accumulation on the tensor cores */
 } phobos_math_t;
 
 typedef enum {
   PHOBOS_PATH_FFMA = 1,
   PHOBOS_PATH_TF32 = 2,
-  PHOBOS_PATH_3XTF32 = 3
+  PHOBOS_PATH_3XTF32 = 3,
+  PHOBOS_PATH_FP16 = 4,
+  PHOBOS_PATH_BF16 = 5
 } phobos_path_t;
 
 /*
  * A plan: which kernel runs and how the problem is tiled.
  *  path            phobos_path_t.
  *  tile_m, tile_n  output tile of one CTA (tile_m = 256 for a 2-CTA pair).
- *  tile_k          K depth of one shared-memory stage.
+ *  tile_k          K depth of one shared-memory stage: 8 for FFMA, 32 for
+ *                  the tf32 paths, 64 for FP16 and BF16 (128 bytes of K
+ *                  either way on the tensor cores).
  *  cluster_m/_n    CTAs per thread-block cluster along M and N (1 x 1 or 2 x 1).
  *  stages          depth of the shared-memory ring.
  *  multicast       1 if operand panels are TMA-multicast inside a cluster.
@@ -105,6 +123,9 @@ typedef enum {
  *                  the workspace; 2 = inside the kernel, which needs
  *                  lda % 4 == 0 and a 16-byte-aligned A, else
  *                  PHOBOS_ERR_UNSUPPORTED).  Identical results either way.
+ *                  FP16 and BF16 always convert A in the pre-pass (0 or 1).
+ *  FP16 and BF16 plans run the tensor-core kernel with its deepest stage ring
+ *  only (stages must equal the planner's value).
  */
 typedef struct {
   int32_t path;

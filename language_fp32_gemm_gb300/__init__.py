@@ -32,13 +32,18 @@ PHOBOS_MATH_DEFAULT = 0
 PHOBOS_MATH_3XTF32 = 1
 PHOBOS_MATH_TF32 = 2
 PHOBOS_MATH_FFMA = 3
+PHOBOS_MATH_FP16 = 4
+PHOBOS_MATH_BF16 = 5
 
 PHOBOS_PATH_FFMA = 1
 PHOBOS_PATH_TF32 = 2
 PHOBOS_PATH_3XTF32 = 3
+PHOBOS_PATH_FP16 = 4
+PHOBOS_PATH_BF16 = 5
 
 MATH_NAMES = {"default": PHOBOS_MATH_DEFAULT, "3xtf32": PHOBOS_MATH_3XTF32,
-              "tf32": PHOBOS_MATH_TF32, "ffma": PHOBOS_MATH_FFMA}
+              "tf32": PHOBOS_MATH_TF32, "ffma": PHOBOS_MATH_FFMA,
+              "fp16": PHOBOS_MATH_FP16, "bf16": PHOBOS_MATH_BF16}
 
 ABI_FUNCTIONS = ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
                  "phobos_check_device", "phobos_set_timing_events", "phobos_kernel_launches",

@@ -35,6 +35,12 @@ cudaError_t launch_split_rows(const float *A, int64_t lda, int M, int K, int Mp,
 // B (K x N, row-major, ldb) -> transposed big/small [Np][Kp] (K-major); zero padding.
 cudaError_t launch_split_cols(const float *B, int64_t ldb, int K, int N, int Np, int Kp,
                               float *big, float *small, cudaStream_t stream);
+// The same layouts with one 16-bit operand (fp16 when bf16 == 0, else bf16),
+// each element rounded to nearest, ties to even.  `out` holds 2-byte elements.
+cudaError_t launch_convert_rows(const float *A, int64_t lda, int M, int K, int Mp, int Kp,
+                                void *out, int bf16, cudaStream_t stream);
+cudaError_t launch_convert_cols(const float *B, int64_t ldb, int K, int N, int Np, int Kp,
+                                void *out, int bf16, cudaStream_t stream);
 // C = beta * C (beta == 0: C = 0 without reading C).
 cudaError_t launch_scale(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);
 
@@ -44,7 +50,7 @@ struct TcArgs {
   float *C;
   int64_t ldc;
   int M, N;
-  int k_block0, k_blocks;  // BK = 32 blocks of this launch
+  int k_block0, k_blocks;  // k blocks (128 bytes of K each) of this launch
   int tiles_m, tiles_n, group_m;
   float alpha, beta;
   int vec_c;
@@ -68,12 +74,19 @@ struct TcArgs {
   unsigned epoch;
   int *err;
 };
-// passes: 1 (tf32) or 3 (split tf32); bn: 128 or 256.
-cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream);
+// Operand types of the tensor-core kernel: tf32 from fp32 containers (one or
+// three passes), or pre-converted fp16 / bf16 (one pass, MMA kind::f16).
+enum TcKind : int { kTcTf32 = 0, kTcF16 = 1, kTcBf16 = 2 };
+// passes: 1 (tf32, fp16, bf16) or 3 (split tf32); bn: 128 or 256.  A k block
+// is 128 bytes of K: 32 fp32 elements, or 64 fp16/bf16 elements, and k_block0
+// and k_blocks count those.
+cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
+                      int kind = kTcTf32);
 int tc_max_stages(int passes, int bn);
 // CTA-pair (cluster of 2, tcgen05 cta_group::2) variant: tiles_m counts
 // 256-row pair tiles; bn: 256.
-cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream);
+cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
+                           int kind = kTcTf32);
 int tc_pair_max_stages(int passes, int bn);
 
 }  // namespace phobos

@@ -45,6 +45,18 @@ int promote_blocks_for(int64_t k) {
 }
 // Single TF32 (bound 2^-10) promotes every K = 1024.
 constexpr int kTf32PromoteBlocks = 32;
+// fp16 / bf16 inputs promote every 8 blocks of 64 (K = 512): a partial's
+// truncating fp32 accumulation then stays within 512 * 2^-23 = 2^-14 of
+// sum|a||b|, far inside the inputs' own rounding (2^-11, 2^-8).
+constexpr int kHalfPromoteBlocks = 8;
+
+bool half_path(int path) { return path == PHOBOS_PATH_FP16 || path == PHOBOS_PATH_BF16; }
+// K elements in one 128-byte k block of a tensor-core path.
+int tc_bk(int path) { return half_path(path) ? 2 * kTcBK : kTcBK; }
+int tc_elem_bytes(int path) { return half_path(path) ? 2 : 4; }
+int tc_kind(int path) {
+  return path == PHOBOS_PATH_FP16 ? kTcF16 : path == PHOBOS_PATH_BF16 ? kTcBf16 : kTcTf32;
+}
 // Tail split: at most this many K pieces per tile, each at least this many K blocks.
 constexpr int kMaxTailSplit = 8;
 constexpr int kMinPieceBlocks = 4;
@@ -162,14 +174,20 @@ phobos_status_t get_encoder() {
   return PHOBOS_OK;
 }
 
-// Tensor map of a K-major buffer [rows][kp] fp32, boxes of 32 x box_rows, 128B swizzle.
-phobos_status_t make_kmajor_map(CUtensorMap *map, const float *base, int64_t rows, int64_t kp,
-                                int box_rows) {
+// Tensor map of a K-major buffer [rows][kp] of the kernel's operand type
+// (fp32 containers for tf32, or fp16 / bf16): boxes of one 128-byte k block
+// x box_rows, 128B swizzle.
+phobos_status_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t rows, int64_t kp,
+                                int box_rows, int kind = kTcTf32) {
+  const int elem = kind == kTcTf32 ? 4 : 2;
+  const CUtensorMapDataType type = kind == kTcTf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : kind == kTcF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kp) * 4};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kp) * elem};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
+  CUresult r = g_encode(map, type, 2, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -201,9 +219,10 @@ phobos_status_t check_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int64_
   return PHOBOS_OK;
 }
 
-size_t tc_workspace(int64_t M, int64_t N, int64_t K, int bm, int bn, int passes) {
-  const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
-  const int64_t a = round_up(Mp * Kp * 4, 256), b = round_up(Np * Kp * 4, 256);
+size_t tc_workspace(int64_t M, int64_t N, int64_t K, int bm, int bn, int passes, int path) {
+  const int e = tc_elem_bytes(path);
+  const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, tc_bk(path));
+  const int64_t a = round_up(Mp * Kp * e, 256), b = round_up(Np * Kp * e, 256);
   return static_cast<size_t>((a + b) * (passes == 3 ? 2 : 1));
 }
 
@@ -215,6 +234,8 @@ phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
     case PHOBOS_MATH_FFMA: path = PHOBOS_PATH_FFMA; break;
     case PHOBOS_MATH_TF32: path = PHOBOS_PATH_TF32; break;
     case PHOBOS_MATH_3XTF32: path = PHOBOS_PATH_3XTF32; break;
+    case PHOBOS_MATH_FP16: path = PHOBOS_PATH_FP16; break;
+    case PHOBOS_MATH_BF16: path = PHOBOS_PATH_BF16; break;
     case PHOBOS_MATH_DEFAULT: {
       const double macs = static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
       path = (macs <= static_cast<double>(kFfmaMacLimit) || M < 16 || N < 16) ? PHOBOS_PATH_FFMA
@@ -245,11 +266,11 @@ phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
     p->tile_m = pair ? 2 * kTcBM : kTcBM;
     p->cluster_m = pair ? 2 : 1;
     p->tile_n = bn;
-    p->tile_k = kTcBK;
+    p->tile_k = tc_bk(path);
     p->stages = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
     p->super_m = kDefaultSuper;
     p->super_n = kDefaultSuper;
-    p->workspace_bytes = tc_workspace(M, N, K, p->tile_m, bn, passes);
+    p->workspace_bytes = tc_workspace(M, N, K, p->tile_m, bn, passes, path);
   }
   return PHOBOS_OK;
 }
@@ -259,6 +280,9 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (math == PHOBOS_MATH_FFMA && p.path != PHOBOS_PATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
   if (math == PHOBOS_MATH_TF32 && p.path != PHOBOS_PATH_TF32) return PHOBOS_ERR_INVALID_VALUE;
   if (math == PHOBOS_MATH_3XTF32 && p.path != PHOBOS_PATH_3XTF32) return PHOBOS_ERR_INVALID_VALUE;
+  if (math == PHOBOS_MATH_FP16 && p.path != PHOBOS_PATH_FP16) return PHOBOS_ERR_INVALID_VALUE;
+  if (math == PHOBOS_MATH_BF16 && p.path != PHOBOS_PATH_BF16) return PHOBOS_ERR_INVALID_VALUE;
+  if (math == PHOBOS_MATH_DEFAULT && half_path(p.path)) return PHOBOS_ERR_INVALID_VALUE;
   if (p.cluster_n != 1 || p.multicast != 0 || (p.cluster_m != 1 && p.cluster_m != 2))
     return PHOBOS_ERR_UNSUPPORTED;
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
@@ -269,16 +293,19 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
     if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
       return PHOBOS_ERR_INVALID_VALUE;
     if (p.tile_k != 8 || (p.super_k < K && p.super_k % 8 != 0)) return PHOBOS_ERR_INVALID_VALUE;
-  } else if (p.path == PHOBOS_PATH_TF32 || p.path == PHOBOS_PATH_3XTF32) {
+  } else if (p.path == PHOBOS_PATH_TF32 || p.path == PHOBOS_PATH_3XTF32 || half_path(p.path)) {
     const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
     const bool pair = p.cluster_m == 2;
+    const int bk = tc_bk(p.path);
     if (p.tile_m != (pair ? 2 * kTcBM : kTcBM) || (p.tile_n != 128 && p.tile_n != 256) ||
-        p.tile_k != kTcBK || (pair && p.tile_n != 256))
+        p.tile_k != bk || (pair && p.tile_n != 256))
       return PHOBOS_ERR_INVALID_VALUE;
     const int max_st = pair ? tc_pair_max_stages(passes, p.tile_n) : tc_max_stages(passes, p.tile_n);
     if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
     if (p.a_split == 2 && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
-    if (p.super_k < K && p.super_k % kTcBK != 0) return PHOBOS_ERR_INVALID_VALUE;
+    // 16-bit inputs: pre-converted A, deepest ring
+    if (half_path(p.path) && (p.a_split == 2 || p.stages != max_st)) return PHOBOS_ERR_INVALID_VALUE;
+    if (p.super_k < K && p.super_k % bk != 0) return PHOBOS_ERR_INVALID_VALUE;
     if (round_up(N, p.tile_n) / 32 > 65535) return PHOBOS_ERR_UNSUPPORTED;
   } else {
     return PHOBOS_ERR_INVALID_VALUE;
@@ -360,19 +387,24 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const bool pair = p.cluster_m == 2;
   const int bm = pair ? 2 * kTcBM : kTcBM;
   const int bn = p.tile_n;
-  const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, kTcBK);
+  const bool half = half_path(p.path);
+  const int bk = tc_bk(p.path), elem = tc_elem_bytes(p.path), kind = tc_kind(p.path);
+  const int64_t Mp = round_up(M, bm), Np = round_up(N, bn), Kp = round_up(K, bk);
   // Where A is split: inside the kernel (TMA reads the caller's A directly)
-  // or by the pre-pass into the workspace.
+  // or by the pre-pass into the workspace.  16-bit inputs are always
+  // converted by the pre-pass.
   const bool a_tma_ok = (lda % 4 == 0) && aligned16(A);
   bool a_inline = false;
-  if (p.a_split == 2) {
+  if (half) {
+    if (p.a_split == 2) return PHOBOS_ERR_UNSUPPORTED;
+  } else if (p.a_split == 2) {
     if (!a_tma_ok) return PHOBOS_ERR_UNSUPPORTED;
     a_inline = true;
   } else if (p.a_split == 0) {
     const int max_st = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
     a_inline = a_tma_ok && N <= kInlineSplitMaxN && p.stages == max_st;
   }
-  const int64_t a_bytes = round_up(Mp * Kp * 4, 256), b_bytes = round_up(Np * Kp * 4, 256);
+  const int64_t a_bytes = round_up(Mp * Kp * elem, 256), b_bytes = round_up(Np * Kp * elem, 256);
   const int ops = passes == 3 ? 2 : 1;  // big (+ small)
   // workspace: [B big][B small][A big][A small] (no A part when A is split in-kernel)
   const size_t ops_bytes = static_cast<size_t>(ops * b_bytes + (a_inline ? 0 : ops * a_bytes));
@@ -382,7 +414,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int units = pair ? dev.sm_count / 2 : dev.sm_count;
   const int total_tiles = static_cast<int>((Mp / bm) * (Np / bn));
   const int chunk_blocks_max =
-      static_cast<int>(round_up(p.super_k < K ? p.super_k : K, kTcBK) / kTcBK);
+      static_cast<int>(round_up(p.super_k < K ? p.super_k : K, bk) / bk);
   int tail_split = 1, full_tiles = total_tiles;
   const int tail = units > 0 ? total_tiles % units : 0;
   if (p.tail_split != 1 && tail != 0) {
@@ -418,17 +450,30 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   float *a_big = reinterpret_cast<float *>(base + ops * b_bytes);
   float *a_small = passes == 3 ? reinterpret_cast<float *>(base + ops * b_bytes + a_bytes) : nullptr;
 
-  if (!a_inline) {
-    st = cuda_status(counted(launch_split_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
-                                               static_cast<int>(Mp), static_cast<int>(Kp), a_big,
-                                               a_small, a_tma_ok, stream)));
+  if (half) {
+    st = cuda_status(counted(launch_convert_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
+                                                 static_cast<int>(Mp), static_cast<int>(Kp), a_big,
+                                                 kind == kTcBf16, stream)));
     if (st != PHOBOS_OK) return st;
-  }
-  if (!reuse_b) {
-    st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
-                                               static_cast<int>(Np), static_cast<int>(Kp), b_big,
-                                               b_small, stream)));
-    if (st != PHOBOS_OK) return st;
+    if (!reuse_b) {
+      st = cuda_status(counted(launch_convert_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
+                                                   static_cast<int>(Np), static_cast<int>(Kp), b_big,
+                                                   kind == kTcBf16, stream)));
+      if (st != PHOBOS_OK) return st;
+    }
+  } else {
+    if (!a_inline) {
+      st = cuda_status(counted(launch_split_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
+                                                 static_cast<int>(Mp), static_cast<int>(Kp), a_big,
+                                                 a_small, a_tma_ok, stream)));
+      if (st != PHOBOS_OK) return st;
+    }
+    if (!reuse_b) {
+      st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
+                                                 static_cast<int>(Np), static_cast<int>(Kp), b_big,
+                                                 b_small, stream)));
+      if (st != PHOBOS_OK) return st;
+    }
   }
 
   TcArgs t{};
@@ -439,12 +484,12 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     if ((st = make_kmajor_map_strided(&t.tmap_ab, A, M, K, lda, kTcBM)) != PHOBOS_OK) return st;
     t.tmap_as = t.tmap_ab;
   } else {
-    if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM)) != PHOBOS_OK) return st;
+    if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM, kind)) != PHOBOS_OK) return st;
     t.tmap_as = t.tmap_ab;
     if (passes == 3 && (st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, kTcBM)) != PHOBOS_OK)
       return st;
   }
-  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, b_box)) != PHOBOS_OK) return st;
+  if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, b_box, kind)) != PHOBOS_OK) return st;
   t.tmap_bs = t.tmap_bb;
   if (passes == 3 && (st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, b_box)) != PHOBOS_OK)
     return st;
@@ -461,8 +506,9 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   t.group_m = static_cast<int>(gm);
   t.vec_c = (ldc % 4 == 0) && aligned16(C);
   // Split TF32 needs short TMEM partial sums to stay at fp32 accuracy.
-  t.promote_blocks =
-      passes == 3 ? promote_blocks_for(p.super_k < K ? p.super_k : K) : kTf32PromoteBlocks;
+  t.promote_blocks = passes == 3 ? promote_blocks_for(p.super_k < K ? p.super_k : K)
+                     : half      ? kHalfPromoteBlocks
+                                 : kTf32PromoteBlocks;
   t.sm_count = dev.sm_count;
   t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD") ? 1 : 0;
   t.full_tiles = full_tiles;
@@ -475,22 +521,22 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   t.flags = flags;
   t.epoch = 1;
   t.err = dev.err;
-  const int total_blocks = static_cast<int>(Kp / kTcBK);
+  const int total_blocks = static_cast<int>(Kp / bk);
   if (p.super_k >= K) {
     t.alpha = alpha;
     t.beta = beta;
     t.k_block0 = 0;
     t.k_blocks = total_blocks;
     if (mark(g_ev_start, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
-    st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream)
-                                   : launch_tc(t, passes, bn, p.stages, stream)));
+    st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream, kind)
+                                   : launch_tc(t, passes, bn, p.stages, stream, kind)));
     if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
     return st;
   }
   // cluster split: init leaf C = beta*C, then step leaves C += alpha * A_c B_c
   st = cuda_status(counted(launch_scale(C, ldc, t.M, t.N, beta, stream)));
   if (st == PHOBOS_OK && mark(g_ev_start, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
-  const int chunk_blocks = static_cast<int>(p.super_k / kTcBK);
+  const int chunk_blocks = static_cast<int>(p.super_k / bk);
   for (int kb = 0; st == PHOBOS_OK && kb < total_blocks; kb += chunk_blocks, ++t.epoch) {
     t.alpha = alpha;
     t.beta = 1.0f;
@@ -501,8 +547,8 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
       t.tail_split = t.k_blocks / kMinPieceBlocks >= 2 ? t.k_blocks / kMinPieceBlocks : 1;
       if (t.tail_split == 1) t.full_tiles = total_tiles;
     }
-    st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream)
-                                   : launch_tc(t, passes, bn, p.stages, stream)));
+    st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream, kind)
+                                   : launch_tc(t, passes, bn, p.stages, stream, kind)));
   }
   if (st == PHOBOS_OK && mark(g_ev_stop, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
   return st;
@@ -527,7 +573,7 @@ phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const f
                            const phobos_gemm_plan_t *user_plan, bool reuse_b = false) {
   phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
   if (st != PHOBOS_OK) return st;
-  if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
+  if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_BF16) return PHOBOS_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) return PHOBOS_OK;
   if (!C) return PHOBOS_ERR_INVALID_VALUE;
   const bool products = K > 0 && alpha != 0.0f;
@@ -595,7 +641,7 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, 
                                   int64_t ldc, void *stream_ptr, phobos_math_t math) {
   phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
   if (st != PHOBOS_OK) return st;
-  if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
+  if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_BF16) return PHOBOS_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) return PHOBOS_OK;
   if (!C) return PHOBOS_ERR_INVALID_VALUE;
   const bool products = K > 0 && alpha != 0.0f;

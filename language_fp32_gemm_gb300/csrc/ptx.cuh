@@ -153,6 +153,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Same with 16-bit inputs (kind::f16: fp16 or bf16, the same type for A and
+// B as the instruction descriptor states), K = 16 per instruction.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on mbarrier `bar` when every tcgen05 operation issued so far by
 // this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -187,6 +199,16 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4)                                 // D: f32
          | (2u << 7)                               // A: tf32
          | (2u << 10)                              // B: tf32
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// Instruction descriptor of kind::f16 with an fp32 accumulator. A and B are
+// both fp16 (bf16 = false) or both bf16: one type for the two operands.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
+  return (1u << 4)                                 // D: f32
+         | ((bf16 ? 1u : 0u) << 7)                 // A: f16 (0) or bf16 (1)
+         | ((bf16 ? 1u : 0u) << 10)                // B: the same as A
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
@@ -330,6 +352,16 @@ __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t adesc, u
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -170,10 +170,13 @@ struct RawAPrefetch {
   }
 };
 
-template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT>
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32>
 __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
+  static_assert(KIND == kTcTf32 || (PASSES == 1 && !ASPLIT), "16-bit inputs: one pass, pre-converted");
+  // K elements per 128-byte stage row: 32 fp32/tf32 or 64 fp16/bf16.
+  constexpr int kBKE = KIND == kTcTf32 ? kBK : 2 * kBK;
   constexpr int kHalf = BN / 2;  // columns summed by one epilogue thread
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
           }
           const uint32_t full = full0 + 8u * s;
           const uint32_t af = a_full0 + 8u * s;
-          const int kc = (p.k_block0 + kb) * kBK;
+          const int kc = (p.k_block0 + kb) * kBKE;
           const uint32_t st = tiles + s * S::kStageBytes;
           const uint32_t bt = st + S::kOps * S::kATile;
           mbar_arrive_expect_tx(af, S::kATile);
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             break;
           }
           const uint32_t full = full0 + 8u * s;
-          const int kc = (p.k_block0 + kb) * kBK;
+          const int kc = (p.k_block0 + kb) * kBKE;
           const uint32_t st = tiles + s * S::kStageBytes;
           const uint32_t bt = st + S::kOps * S::kATile;
           if (PAIR) {
@@ -437,7 +440,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_tf32(kTileM, BN);
+      constexpr uint32_t idesc =
+          KIND == kTcTf32 ? idesc_tf32(kTileM, BN) : idesc_f16(kTileM, BN, KIND == kTcBf16);
       int g = 0;       // k blocks consumed: ring slot and phase
       int c_glob = 0;  // partial sums produced: TMEM buffer and its phase
       bool ok = true;
@@ -482,7 +486,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             const uint32_t b_small = b_big + S::kBTile;
 #pragma unroll
             for (int kk = 0; kk < kBK / 8; ++kk) {
-              const uint32_t off = kk * 32u;  // 8 tf32 = 32 bytes along K
+              // one MMA's K slice: 32 bytes (8 tf32, or 16 fp16/bf16)
+              const uint32_t off = kk * 32u;
               const uint64_t dab = desc_kmajor_sw128(a_big + off);
               const uint64_t dbb = desc_kmajor_sw128(b_big + off);
               const uint32_t acc = (first && kk == 0) ? 0u : 1u;
@@ -498,11 +503,16 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
                   mma_tf32(d_tmem, dab, dbs, idesc, 1u);
                   mma_tf32(d_tmem, dab, dbb, idesc, 1u);
                 }
-              } else {
+              } else if (KIND == kTcTf32) {
                 if (PAIR)
                   mma_tf32_pair(d_tmem, dab, dbb, idesc, acc);
                 else
                   mma_tf32(d_tmem, dab, dbb, idesc, acc);
+              } else {
+                if (PAIR)
+                  mma_f16_pair(d_tmem, dab, dbb, idesc, acc);
+                else
+                  mma_f16(d_tmem, dab, dbb, idesc, acc);
               }
             }
             if (PAIR)
@@ -770,11 +780,11 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
   }
 }
 
-template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT>
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32>
 cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
-  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT>;
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND>;
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -805,9 +815,15 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
 }
 
 template <int BN, int PASSES, bool PAIR>
-cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream) {
+cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream, int kind) {
   constexpr int kMax = TcShape<BN, PASSES, PAIR>::max_stages();
   constexpr int kTop = kMax >= 4 ? 4 : kMax;
+  // 16-bit inputs: one pass, pre-converted operands, the deepest ring only.
+  if (kind != kTcTf32) {
+    if (PASSES != 1 || a.a_inline || stages != kTop) return cudaErrorInvalidValue;
+    return kind == kTcF16 ? launch_one<BN, 1, kTop, PAIR, false, kTcF16>(a, stream)
+                          : launch_one<BN, 1, kTop, PAIR, false, kTcBf16>(a, stream);
+  }
   // In-kernel A split: always the deepest ring.
   if (a.a_inline) return launch_one<BN, PASSES, kTop, PAIR, true>(a, stream);
   if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2), PAIR, false>(a, stream);
@@ -831,17 +847,21 @@ int max_stages_of(int passes, int bn) {
 int tc_max_stages(int passes, int bn) { return max_stages_of<false>(passes, bn); }
 int tc_pair_max_stages(int passes, int bn) { return max_stages_of<true>(passes, bn); }
 
-cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream) {
-  if (passes == 3 && bn == 256) return launch_stages<256, 3, false>(a, stages, stream);
-  if (passes == 3 && bn == 128) return launch_stages<128, 3, false>(a, stages, stream);
-  if (passes == 1 && bn == 256) return launch_stages<256, 1, false>(a, stages, stream);
-  if (passes == 1 && bn == 128) return launch_stages<128, 1, false>(a, stages, stream);
+cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
+                      int kind) {
+  if (kind != kTcTf32 && kind != kTcF16 && kind != kTcBf16) return cudaErrorInvalidValue;
+  if (passes == 3 && bn == 256) return launch_stages<256, 3, false>(a, stages, stream, kind);
+  if (passes == 3 && bn == 128) return launch_stages<128, 3, false>(a, stages, stream, kind);
+  if (passes == 1 && bn == 256) return launch_stages<256, 1, false>(a, stages, stream, kind);
+  if (passes == 1 && bn == 128) return launch_stages<128, 1, false>(a, stages, stream, kind);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream) {
-  if (passes == 3 && bn == 256) return launch_stages<256, 3, true>(a, stages, stream);
-  if (passes == 1 && bn == 256) return launch_stages<256, 1, true>(a, stages, stream);
+cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
+                           int kind) {
+  if (kind != kTcTf32 && kind != kTcF16 && kind != kTcBf16) return cudaErrorInvalidValue;
+  if (passes == 3 && bn == 256) return launch_stages<256, 3, true>(a, stages, stream, kind);
+  if (passes == 1 && bn == 256) return launch_stages<256, 1, true>(a, stages, stream, kind);
   return cudaErrorInvalidValue;
 }
 

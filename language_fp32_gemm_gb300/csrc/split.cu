@@ -10,6 +10,13 @@
 // the buffers.  The pages convert fp32 operands before the tensor cores too,
 // and note the single conversion is lossy ("Show HN: Phobos", footnote 14);
 // the two-term split recovers fp32-level products.
+//
+// 16-bit inputs ("Show HN: Phobos", "Side-quest: Cheating": cast to a 16-bit
+// type before the tensor cores): the same two layouts hold one fp16 or bf16
+// value per element, rounded to nearest with ties to even.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -79,6 +86,67 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float *__restrict
   }
 }
 
+template <bool BF16>
+__device__ __forceinline__ unsigned short to_16bit(float x) {
+  if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+// A (M x K) -> [Mp][Kp] 16-bit, four elements (8 bytes) per thread.
+template <bool BF16>
+__global__ void __launch_bounds__(256) convert_rows_kernel(const float *__restrict__ A, int64_t lda,
+                                                           int M, int K, int Mp, int Kp,
+                                                           unsigned short *__restrict__ out, int vec) {
+  const int64_t groups_per_row = Kp / 4;
+  const int64_t total = static_cast<int64_t>(Mp) * groups_per_row;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(g / groups_per_row);
+    const int k = static_cast<int>(g - static_cast<int64_t>(i) * groups_per_row) * 4;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < M) {
+      const float *src = A + static_cast<int64_t>(i) * lda + k;
+      if (vec && k + 3 < K) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (k + t < K) x[t] = __ldg(src + t);
+      }
+    }
+    uint2 w;
+    w.x = static_cast<uint32_t>(to_16bit<BF16>(x[0])) | (static_cast<uint32_t>(to_16bit<BF16>(x[1])) << 16);
+    w.y = static_cast<uint32_t>(to_16bit<BF16>(x[2])) | (static_cast<uint32_t>(to_16bit<BF16>(x[3])) << 16);
+    *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(i) * Kp + k) = w;
+  }
+}
+
+// B (K x N) -> K-major [Np][Kp] 16-bit through a 32 x 32 shared-memory tile.
+template <bool BF16>
+__global__ void __launch_bounds__(256) convert_cols_kernel(const float *__restrict__ B, int64_t ldb,
+                                                           int K, int N, int Kp,
+                                                           unsigned short *__restrict__ out) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32;
+  const int n0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;  // 0..7
+#pragma unroll
+  for (int r = 0; r < 32; r += 8) {
+    const int k = k0 + ty + r;
+    const int n = n0 + tx;
+    tile[ty + r][tx] = (k < K && n < N) ? __ldg(B + static_cast<int64_t>(k) * ldb + n) : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 32; r += 8) {
+    const int n = n0 + ty + r;
+    const int k = k0 + tx;
+    out[static_cast<int64_t>(n) * Kp + k] = to_16bit<BF16>(tile[tx][ty + r]);
+  }
+}
+
 __global__ void __launch_bounds__(256) scale_kernel(float *C, int64_t ldc, int M, int N,
                                                     float beta) {
   const int64_t total = static_cast<int64_t>(M) * N;
@@ -113,6 +181,29 @@ cudaError_t launch_split_cols(const float *B, int64_t ldb, int K, int N, int Np,
                               float *big, float *small, cudaStream_t stream) {
   dim3 grid(Kp / 32, Np / 32);
   split_cols_kernel<<<grid, 256, 0, stream>>>(B, ldb, K, N, Kp, big, small);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_rows(const float *A, int64_t lda, int M, int K, int Mp, int Kp,
+                                void *out, int bf16, cudaStream_t stream) {
+  const int64_t groups = static_cast<int64_t>(Mp) * (Kp / 4);
+  const int vec = (lda % 4 == 0) && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
+  unsigned short *o = static_cast<unsigned short *>(out);
+  if (bf16)
+    convert_rows_kernel<true><<<grid_for(groups, 256), 256, 0, stream>>>(A, lda, M, K, Mp, Kp, o, vec);
+  else
+    convert_rows_kernel<false><<<grid_for(groups, 256), 256, 0, stream>>>(A, lda, M, K, Mp, Kp, o, vec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_cols(const float *B, int64_t ldb, int K, int N, int Np, int Kp,
+                                void *out, int bf16, cudaStream_t stream) {
+  dim3 grid(Kp / 32, Np / 32);
+  unsigned short *o = static_cast<unsigned short *>(out);
+  if (bf16)
+    convert_cols_kernel<true><<<grid, 256, 0, stream>>>(B, ldb, K, N, Kp, o);
+  else
+    convert_cols_kernel<false><<<grid, 256, 0, stream>>>(B, ldb, K, N, Kp, o);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,9 @@ Acceptance rule (the error scale is the oracle's ``den``):
     err = max_ij |C[i,j] - ref64[i,j]| / den[i,j]
 with entries where den == 0 required to equal ``float32(ref64)`` exactly and
 any NaN failing.  Bounds: 2**-20 for the split-TF32 (3xTF32), FFMA and
-K-chunked modes, 2**-10 for single-pass TF32.
+K-chunked modes, 2**-10 for single-pass TF32.  The fp16/bf16-input mode is
+checked against the oracle of its rounded inputs (``round_inputs``) with
+2**-13, and against the fp32 inputs with 2**-9 (fp16) or 2**-6 (bf16).
 """
 import ctypes
 import os
@@ -26,6 +28,15 @@ from . import build as _build
 
 TOL_FP32 = 2.0 ** -20   # 3xTF32, FFMA, K-chunked
 TOL_TF32 = 2.0 ** -10   # single-pass TF32
+# fp16 / bf16 inputs (the reduced-precision tensor-core mode).  Against the
+# oracle of the rounded inputs, only the fp32 accumulation differs: partial sums
+# of K = 512 added by truncating fp32 adds (<= 512 * 2^-23 = 2^-14 of sum|ab|),
+# then added with round-to-nearest (< 2^-18 for K up to 2^16) and scaled once.
+TOL_HALF_ACC = 2.0 ** -13
+# Against the oracle of the fp32 inputs, each product r(a) r(b) differs from a b
+# by at most (2u + u^2)|ab|, u = 2^-11 (fp16) or 2^-8 (bf16), plus the above.
+TOL_FP16 = 2.0 ** -9
+TOL_BF16 = 2.0 ** -6
 
 _lib = None
 
@@ -165,3 +176,29 @@ def max_rel_error(C, ref64, den):
 def ref32(ref64):
     """Round the fp64 oracle result to fp32 (round to nearest even)."""
     return np.asarray(ref64, dtype=np.float64).astype(np.float32)
+
+
+def round_inputs(x, fmt):
+    """Each fp32 value rounded to the nearest fp16 or bf16 value, ties to even,
+    returned as fp32 (both types embed exactly in fp32).
+
+    This is the input cast of the reduced-precision tensor-core mode: "Show HN:
+    Phobos", section "Side-quest: Cheating", casts the fp32 data to a 16-bit
+    type before the tensor cores and keeps an fp32 accumulator.  The mode's
+    result is the plain definition applied to the rounded inputs:
+    sgemm(round_inputs(A), round_inputs(B), C_old, alpha, beta).
+
+    fp16 uses numpy's IEEE binary16 conversion (a library step).  bf16 is the
+    upper half of the fp32 bit pattern, rounded to nearest with ties to even on
+    the discarded 16 bits.  Finite inputs only.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if fmt == "fp16":
+        return x.astype(np.float16).astype(np.float32)
+    if fmt == "bf16":
+        bits = x.view(np.uint32).astype(np.uint64)
+        keep_odd = (bits >> 16) & 1          # ties go to the even upper half
+        r = ((bits + 0x7FFF + keep_odd) >> 16) << 16
+        return r.astype(np.uint32).view(np.float32)
+    raise ValueError("fmt must be 'fp16' or 'bf16'")
+

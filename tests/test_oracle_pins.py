@@ -89,3 +89,59 @@ def test_error_metric():
     assert oracle.max_rel_error(np.array([np.nan, 0.0, -2.0]), ref, den) == float("inf")
     assert oracle.max_rel_error(np.array([1.0, 0.0, -1.0]), ref, den) == 0.25
     assert oracle.TOL_FP32 == 2.0 ** -20 and oracle.TOL_TF32 == 2.0 ** -10
+
+
+def _nearest_even(x, table_bits, to_float):
+    """Brute force: the value of the 16-bit table nearest to each x, ties to the
+    even bit pattern, found by searching every finite value of the type."""
+    with np.errstate(invalid="ignore"):
+        vals = to_float(table_bits).astype(np.float64)
+    ok = np.isfinite(vals)
+    vals, bits = vals[ok], table_bits[ok]
+    order = np.argsort(vals, kind="stable")
+    vals, bits = vals[order], bits[order]
+    keep = np.concatenate(([True], np.diff(vals) != 0))  # +0 and -0 are one value
+    vals, bits = vals[keep], bits[keep]
+    out = np.empty(x.shape, dtype=np.float64)
+    for n, v in enumerate(x.astype(np.float64)):
+        j = int(np.searchsorted(vals, v))
+        cands = [c for c in (j - 1, j) if 0 <= c < len(vals)]
+        best = min(cands, key=lambda c: (abs(vals[c] - v), int(bits[c]) & 1))
+        out[n] = vals[best]
+    return out
+
+
+def _probe_values():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([
+        rng.standard_normal(3000),
+        rng.uniform(-1, 1, 3000) * 2.0 ** rng.integers(-20, 15, 3000),
+        # exact ties of both types: 1 + (2j+1) * 2^-11 and 1 + (2j+1) * 2^-8
+        1 + (2 * np.arange(40) + 1) * 2.0 ** -11, -(1 + (2 * np.arange(40) + 1) * 2.0 ** -8),
+        [0.0, 1.0, -1.0, 0.5, 65504.0, 2.0 ** -14, 3.0 * 2 ** -9],
+    ])
+    return x.astype(np.float32)
+
+
+def test_round_inputs_fp16_is_nearest_even():
+    """fp16 rounding of the oracle equals an exhaustive nearest-value search."""
+    x = _probe_values()
+    x = x[np.abs(x) <= 65504]
+    table = np.arange(1 << 16, dtype=np.uint16)
+    want = _nearest_even(x, table, lambda b: b.view(np.float16))
+    got = oracle.round_inputs(x, "fp16").astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+def test_round_inputs_bf16_is_nearest_even():
+    """bf16 rounding of the oracle equals an exhaustive nearest-value search."""
+    x = _probe_values()
+    table = np.arange(1 << 16, dtype=np.uint32)
+    want = _nearest_even(x, table, lambda b: (b << 16).astype(np.uint32).view(np.float32))
+    got = oracle.round_inputs(x, "bf16").astype(np.float64)
+    assert np.array_equal(got, want)
+    # values a bf16 holds exactly are unchanged, and the rounding is monotone
+    exact = np.arange(-255, 256, dtype=np.float32) * 0.25  # 8 significant bits at most
+    assert np.array_equal(oracle.round_inputs(exact, "bf16"), exact)
+    s = np.sort(x)
+    assert np.all(np.diff(oracle.round_inputs(s, "bf16").astype(np.float64)) >= 0)
