@@ -304,7 +304,8 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
     if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
     if (p.a_split == 2 && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
     // 16-bit inputs: pre-converted A, deepest ring
-    if (half_path(p.path) && (p.a_split == 2 || p.stages != max_st)) return PHOBOS_ERR_INVALID_VALUE;
+    if (half_path(p.path) && (p.a_split == 2 || (p.stages != max_st && p.stages != 4)))
+      return PHOBOS_ERR_INVALID_VALUE;
     if (p.super_k < K && p.super_k % bk != 0) return PHOBOS_ERR_INVALID_VALUE;
     if (round_up(N, p.tile_n) / 32 > 65535) return PHOBOS_ERR_UNSUPPORTED;
   } else {

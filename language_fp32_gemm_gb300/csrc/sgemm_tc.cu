@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(KIND == kTcTf32 || (PASSES == 1 && !ASPLIT), "16-bit inputs: one pass, pre-converted");
+  static_assert((4 * STAGES + 5) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   // K elements per 128-byte stage row: 32 fp32/tf32 or 64 fp16/bf16.
   constexpr int kBKE = KIND == kTcTf32 ? kBK : 2 * kBK;
   constexpr int kHalf = BN / 2;  // columns summed by one epilogue thread
@@ -817,15 +818,26 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
 template <int BN, int PASSES, bool PAIR>
 cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream, int kind) {
   constexpr int kMax = TcShape<BN, PASSES, PAIR>::max_stages();
-  constexpr int kTop = kMax >= 4 ? 4 : kMax;
+  // Up to 6 stages: one-pass kernels (TF32, fp16, bf16) have 32 KiB stages and
+  // only 512 MMA cycles per stage, so they need the deeper ring to cover a
+  // load's latency; the barrier block (4 * 6 + 5 barriers) still fits its
+  // 256 bytes.
+  constexpr int kTop = kMax >= 6 ? 6 : kMax;
   // 16-bit inputs: one pass, pre-converted operands, the deepest ring only.
   if (kind != kTcTf32) {
-    if (PASSES != 1 || a.a_inline || stages != kTop) return cudaErrorInvalidValue;
-    return kind == kTcF16 ? launch_one<BN, 1, kTop, PAIR, false, kTcF16>(a, stream)
-                          : launch_one<BN, 1, kTop, PAIR, false, kTcBf16>(a, stream);
+    if (PASSES != 1 || a.a_inline) return cudaErrorInvalidValue;
+    if (stages == kTop)
+      return kind == kTcF16 ? launch_one<BN, 1, kTop, PAIR, false, kTcF16>(a, stream)
+                            : launch_one<BN, 1, kTop, PAIR, false, kTcBf16>(a, stream);
+    if (stages == 4 && kMax >= 4)
+      return kind == kTcF16 ? launch_one<BN, 1, (kMax >= 4 ? 4 : 2), PAIR, false, kTcF16>(a, stream)
+                            : launch_one<BN, 1, (kMax >= 4 ? 4 : 2), PAIR, false, kTcBf16>(a, stream);
+    return cudaErrorInvalidValue;
   }
   // In-kernel A split: always the deepest ring.
   if (a.a_inline) return launch_one<BN, PASSES, kTop, PAIR, true>(a, stream);
+  if (stages >= 6 && kMax >= 6) return launch_one<BN, PASSES, (kMax >= 6 ? 6 : 2), PAIR, false>(a, stream);
+  if (stages >= 5 && kMax >= 5) return launch_one<BN, PASSES, (kMax >= 5 ? 5 : 2), PAIR, false>(a, stream);
   if (stages >= 4 && kMax >= 4) return launch_one<BN, PASSES, (kMax >= 4 ? 4 : 2), PAIR, false>(a, stream);
   if (stages >= 3 && kMax >= 3) return launch_one<BN, PASSES, (kMax >= 3 ? 3 : 2), PAIR, false>(a, stream);
   if (stages >= 2) return launch_one<BN, PASSES, 2, PAIR, false>(a, stream);
@@ -839,7 +851,7 @@ int max_stages_of(int passes, int bn) {
   if (passes == 3 && bn == 128) m = TcShape<128, 3, PAIR>::max_stages();
   if (passes == 1 && bn == 256) m = TcShape<256, 1, PAIR>::max_stages();
   if (passes == 1 && bn == 128) m = TcShape<128, 1, PAIR>::max_stages();
-  return m > 4 ? 4 : m;
+  return m > 6 ? 6 : m;
 }
 
 }  // namespace
