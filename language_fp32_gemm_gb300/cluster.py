@@ -468,6 +468,8 @@ def pod_main(host, port, node, device=DEVICE_CUDA, arena_bytes=None, heartbeat=0
                     run_segment(blob, job, arena, device, staged, stored, host_gemm, staging_bytes)
             gen = g
     except BaseException as e:
+        if store.check(["dead/%d" % node]):
+            return  # declared dead meanwhile: the scheduler has re-planned this node's work
         store.set("fail/%d" % node, "%s: %s" % (type(e).__name__, e))
         raise
     finally:
@@ -552,7 +554,9 @@ class Scheduler:
             stored = {o for o, t in ids.items() if self.store.check(["stored/%016x" % t])}
             if len(stored) == len(ids):
                 break
-            for n in range(self.nodes):
+            # A node already declared dead may still report a failure (its pod
+            # refuses to write into C once dead); its work has been re-planned.
+            for n in self.live:
                 if self.store.check(["fail/%d" % n]):
                     raise RuntimeError("node %d failed: %s" % (n, _s(self.store.get("fail/%d" % n))))
             now = time.time()
@@ -578,8 +582,17 @@ class Scheduler:
                     pm, pn = divmod(o, gn)
                     if self.store.check(["staged/%016x" % ids[o]]):
                         r0, c0 = pm * sm, pn * sn
-                        _finish_staged(job, ids[o], r0, c0, min(sm, job.M - r0), min(sn, job.N - c0))
-                        self.store.set("stored/%016x" % ids[o], "scheduler")
+                        try:
+                            _finish_staged(job, ids[o], r0, c0, min(sm, job.M - r0), min(sn, job.N - c0))
+                            self.store.set("stored/%016x" % ids[o], "scheduler")
+                        except FileNotFoundError:
+                            # The pod, still running, finished phase 2 itself
+                            # and removed the side file: the same bytes are in C.
+                            deadline_store = time.time() + self.timeout
+                            while not self.store.check(["stored/%016x" % ids[o]]):
+                                if time.time() > deadline_store:
+                                    raise RuntimeError("tile %d lost its side file but was not stored" % o)
+                                time.sleep(poll)
                     else:
                         redo.append(o)
                 if redo:
@@ -603,10 +616,14 @@ def _pod_entry(host, port, node, device, arena_bytes, heartbeat, host_gemm, exit
 
 
 def run_local(job, nodes, budget, device=DEVICE_CUDA, autotune=False, heartbeat=0.1,
-              heartbeat_timeout=5.0, host_gemm=None, fail=None, staging_bytes=0, deadline=3600.0):
+              heartbeat_timeout=5.0, host_gemm=None, fail=None, staging_bytes=0, deadline=3600.0,
+              heartbeat_overrides=None):
     """Run `job` on `nodes` pod processes of this machine, with the scheduler here.
 
     ``fail`` maps a node to the ``exit_at`` of its pod (see :func:`pod_main`).
+    ``heartbeat_overrides`` maps a node to its own heartbeat interval (a node
+    that beats slower than ``heartbeat_timeout`` is declared dead while it
+    still runs).
     Pods are started with the "spawn" method, so a script that calls this
     must do so under ``if __name__ == "__main__":``.
     ``host_gemm`` (picklable; host device only) computes the leaves of the
@@ -626,7 +643,8 @@ def run_local(job, nodes, budget, device=DEVICE_CUDA, autotune=False, heartbeat=
     procs = []
     for n in range(nodes):
         exit_at = (fail or {}).get(n)
-        pr = ctx.Process(target=_pod_entry, args=(sched.host, sched.port, n, device, None, heartbeat,
+        beat = (heartbeat_overrides or {}).get(n, heartbeat)
+        pr = ctx.Process(target=_pod_entry, args=(sched.host, sched.port, n, device, None, beat,
                                                   host_gemm, exit_at, staging_bytes))
         pr.start()
         procs.append(pr)

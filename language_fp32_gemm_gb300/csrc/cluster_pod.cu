@@ -34,6 +34,7 @@
 
 #include "../../include/phobos_cluster.h"
 #include "cluster_internal.h"
+#include "internal.h"
 
 namespace phobos {
 namespace cluster {
@@ -164,7 +165,12 @@ class Pod {
       if (stage_out_) cudaFreeHost(stage_out_);
       if (copy_in_) cudaStreamDestroy(copy_in_);
       if (copy_out_) cudaStreamDestroy(copy_out_);
-      if (compute_ && own_compute_) cudaStreamDestroy(compute_);
+      if (compute_ && own_compute_) {
+        // the leaves' workspace is cached per stream: free it with the stream
+        phobos::release_stream_workspace(compute_);
+        cudaStreamSynchronize(compute_);
+        cudaStreamDestroy(compute_);
+      }
       if (base_) cudaFree(base_);
     } else {
       std::free(base_);

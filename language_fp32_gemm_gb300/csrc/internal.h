@@ -7,6 +7,8 @@
 
 #include <cstdint>
 
+#include "../../include/phobos_gemm.h"
+
 namespace phobos {
 
 // ---------------------------------------------------------------- FFMA path
@@ -88,5 +90,9 @@ int tc_max_stages(int passes, int bn);
 cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
                            int kind = kTcTf32);
 int tc_pair_max_stages(int passes, int bn);
+
+// Frees the workspace cached for `stream` on the current device (stream-ordered);
+// for code in this library that destroys a stream it created.
+phobos_status_t release_stream_workspace(cudaStream_t stream);
 
 }  // namespace phobos

@@ -162,6 +162,24 @@ phobos_status_t ensure_buffer(Buffer &b, size_t bytes, cudaStream_t stream) {
   return PHOBOS_OK;
 }
 
+}  // namespace
+
+// The workspace cached for `stream` on the current device, released
+// stream-ordered: for callers that are about to destroy a stream they made.
+phobos_status_t release_stream_workspace(cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  auto it = g_workspaces.find({device, reinterpret_cast<uintptr_t>(stream)});
+  if (it == g_workspaces.end()) return PHOBOS_OK;
+  phobos_status_t st = PHOBOS_OK;
+  if (it->second.ptr && cudaFreeAsync(it->second.ptr, stream) != cudaSuccess) st = PHOBOS_ERR_CUDA;
+  g_workspaces.erase(it);
+  return st;
+}
+
+namespace {
+
 phobos_status_t get_encoder() {
   if (g_encode) return PHOBOS_OK;
   void *fn = nullptr;

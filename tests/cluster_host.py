@@ -27,6 +27,14 @@ def host_gemm(m, n, k, alpha, a, lda, b, ldb, beta, c, ldc):
     C[...] = (float(alpha) * (A @ B) + float(beta) * C.astype(np.float64)).astype(np.float32)
 
 
+def slow_host_gemm(m, n, k, alpha, a, lda, b, ldb, beta, c, ldc):
+    """host_gemm that takes 0.15 s per leaf, so a pod is still busy when the
+    scheduler gives up on its heartbeat."""
+    import time
+    time.sleep(0.15)
+    host_gemm(m, n, k, alpha, a, lda, b, ldb, beta, c, ldc)
+
+
 def write_job(tmp, M, N, K, alpha, beta, seed, lo, hi=None):
     """Seeded A, B, C_old as raw fp32 files under `tmp`; returns (Job, A, B, C_old)."""
     import seeded_inputs as si

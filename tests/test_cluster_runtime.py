@@ -109,3 +109,20 @@ def test_lost_node_is_replanned(tmp_path, phase):
     else:
         assert redo == first[1:]  # the staged one was finished from its side file
     check(job, A, B, C0)
+
+
+def test_slow_node_declared_dead_stops_cleanly(tmp_path):
+    """A pod that still runs but stops heart-beating is declared dead.
+
+    Its unstored outputs are re-planned. The pod refuses to write into C from
+    then on, since its staged hook sees the dead mark, and it leaves without
+    reporting a failure. The result is complete and correct (beta != 0, so C
+    is read in place)."""
+    job, A, B, C0 = cluster_host.write_job(tmp_path, 256, 256, 96, 1.0, 0.5, seed=46, lo=(64, 64, 32))
+    sc = cluster.run_local(job, 3, budget=1 << 20, device=cluster.DEVICE_HOST,
+                           host_gemm=cluster_host.slow_host_gemm, heartbeat_timeout=1.0,
+                           heartbeat_overrides={1: 30.0}, deadline=300)
+    assert sc.replans >= 1
+    assert any(kind == "replan" and lost == [1] for kind, lost, *_ in sc.log)
+    assert sc.exitcodes == [0, 0, 0]
+    check(job, A, B, C0)
