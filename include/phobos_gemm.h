@@ -93,7 +93,7 @@ typedef enum {
  * A plan: which kernel runs and how the problem is tiled.
  *  path            phobos_path_t.
  *  tile_m, tile_n  output tile of one CTA (tile_m = 256 for a 2-CTA pair).
- *  tile_k          K depth of one shared-memory stage: 8 for FFMA, 32 for
+ *  tile_k          K depth of one shared-memory stage: 16 for FFMA, 32 for
  *                  the tf32 paths, 64 for FP16 and BF16 (128 bytes of K
  *                  either way on the tensor cores).
  *  cluster_m/_n    CTAs per thread-block cluster along M and N (1 x 1 or 2 x 1).

@@ -271,7 +271,7 @@ phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
     const int t = (M >= 1024 && N >= 1024) ? 128 : 64;
     p->tile_m = t;
     p->tile_n = t;
-    p->tile_k = 8;
+    p->tile_k = 16;
     p->stages = 2;
     p->super_m = round_up(kDefaultSuper, t);
     p->super_n = round_up(kDefaultSuper, t);
@@ -310,7 +310,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
     if (p.cluster_m != 1) return PHOBOS_ERR_UNSUPPORTED;
     if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
       return PHOBOS_ERR_INVALID_VALUE;
-    if (p.tile_k != 8 || (p.super_k < K && p.super_k % 8 != 0)) return PHOBOS_ERR_INVALID_VALUE;
+    if (p.tile_k != 16 || (p.super_k < K && p.super_k % 8 != 0)) return PHOBOS_ERR_INVALID_VALUE;
   } else if (p.path == PHOBOS_PATH_TF32 || p.path == PHOBOS_PATH_3XTF32 || half_path(p.path)) {
     const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
     const bool pair = p.cluster_m == 2;
