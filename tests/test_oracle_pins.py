@@ -145,3 +145,26 @@ def test_round_inputs_bf16_is_nearest_even():
     assert np.array_equal(oracle.round_inputs(exact, "bf16"), exact)
     s = np.sort(x)
     assert np.all(np.diff(oracle.round_inputs(s, "bf16").astype(np.float64)) >= 0)
+
+
+@pytest.mark.parametrize("mutant", ["truncate", "ties_away", "fp16_truncate"])
+def test_rounding_pins_catch_mutants(mutant):
+    """Plausible mistakes in the 16-bit input rounding fail the exhaustive pins."""
+    x = _probe_values()
+    if mutant == "fp16_truncate":
+        x = x[np.abs(x) <= 65504]
+        table = np.arange(1 << 16, dtype=np.uint16)
+        want = _nearest_even(x, table, lambda b: b.view(np.float16))
+        # round toward zero: drop the 13 low mantissa bits (normal range only)
+        bits = x.view(np.uint32)
+        bad = ((bits >> 13) << 13).view(np.float32).astype(np.float16).astype(np.float64)
+    else:
+        table = np.arange(1 << 16, dtype=np.uint32)
+        want = _nearest_even(x, table, lambda b: (b << 16).astype(np.uint32).view(np.float32))
+        bits = x.view(np.uint32).astype(np.uint64)
+        if mutant == "truncate":
+            r = (bits >> 16) << 16
+        else:  # ties away from zero instead of to even
+            r = ((bits + 0x8000) >> 16) << 16
+        bad = r.astype(np.uint32).view(np.float32).astype(np.float64)
+    assert not np.array_equal(bad, want), mutant
