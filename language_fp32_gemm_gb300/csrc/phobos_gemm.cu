@@ -36,11 +36,14 @@ constexpr int64_t kDefaultSuper = 4096;                 // super-tile edge (rast
 //   partials of 2 blocks: 6.9e-7 at K = 64, 3.2e-7 at K = 256, 1.9e-7 at K = 512
 //   partials of 1 block:  3.7e-7 at K = 64, 2.4e-7 at K = 128
 // while shorter partials cost speed (8192^3: 367, 355, 322, 204 TFLOP/s).  So
-// the length follows K, keeping every case near 4e-7 or below.
+// the length follows K, keeping every case at 5e-7 or below.  Two partials
+// are also the slack the next tile's MMAs have while the accumulator warps
+// store a tile, so above K = 1024 the longer partials are used: 8 blocks
+// measured 4.7e-7 at K = 1025, 3.3e-7 at K = 2000 (2 M outputs each).
 int promote_blocks_for(int64_t k) {
   if (k <= 128) return 1;
   if (k <= 512) return 2;
-  if (k <= 2048) return 4;
+  if (k <= 1024) return 4;
   return 8;
 }
 // Single TF32 (bound 2^-10) promotes every K = 1024.

@@ -307,7 +307,7 @@ def test_host_buffer_entry_point_in_bands(dev, beta):
 
 # ----------------------------- split-TF32 accuracy where it is tightest
 
-@pytest.mark.parametrize("K", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("K", [32, 64, 128, 256, 512, 1025, 1100, 2000, 2048])
 def test_split_tf32_short_k_stress(dev, K):
     # The tensor core truncates while it accumulates a TMEM partial sum; the
     # error relative to sum|a||b| is largest when K spans few partials.  Two
