@@ -47,6 +47,10 @@ cudaError_t launch_convert_cols(const float *B, int64_t ldb, int K, int N, int N
 cudaError_t launch_scale(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t stream);
 
 // ------------------------------------------------------- tensor-core path
+// Shortest K piece (in K blocks) of a tail tile split among workers, and the
+// most workers that can share the tail of one launch.
+constexpr int kMinPieceBlocks = 4;
+constexpr int kMaxTailUnits = 160;
 struct TcArgs {
   CUtensorMap tmap_ab, tmap_as, tmap_bb, tmap_bs;  // K-major operand maps
   float *C;
@@ -59,13 +63,19 @@ struct TcArgs {
   int promote_blocks;  // K blocks per TMEM partial sum before it is added into registers
   int sm_count;        // SMs of the device: the persistent grid size
   int withhold_first_load;  // testing only: skip the first operand load (a wait then expires)
-  // Split of the last, partial wave along K (0 or 1 = off).  Tiles
-  // [0, full_tiles) are computed whole; each of the remaining tiles is cut
-  // into tail_split K pieces.  Piece p > 0 writes its sum to partials slot
-  // (tile - full_tiles) * (tail_split - 1) + p - 1 (tile_m x BN floats), and
-  // each accumulator warp stores `epoch` into flags[(slot * 2 + cta rank) * 8
-  // + warp - 2]; piece 0 adds the slots in order and stores C.
-  int full_tiles, tail_split;
+  // Split of the last, partial wave along K.  Tiles [0, full_tiles) are
+  // computed whole, strided over the workers (CTAs, or CTA pairs).  The K
+  // blocks of the remaining tiles, laid end to end, are dealt evenly to
+  // workers 0 .. tail_units-1 (0 = no split): worker w's share runs from tail
+  // tile tail_tile[w], K block tail_k[w] (tile counted from full_tiles, k in
+  // [0, k_blocks)) to the start of worker w + 1's share; entry tail_units is
+  // (tail tiles, 0).  A piece that starts at k = 0 owns its tile; a later
+  // piece is the first piece of its worker w, writes its sum to partials slot
+  // w (tile_m x BN floats), and each accumulator warp stores `epoch` into
+  // flags[(w * 2 + cta rank) * 8 + warp - 2]; the owner adds the slots in K
+  // order and stores C.
+  int full_tiles, tail_units;
+  int tail_tile[kMaxTailUnits + 1], tail_k[kMaxTailUnits + 1];
   int grid_units;  // CTAs (pairs) to launch; 0 = min(tiles, SMs (pairs))
   // 1: tmap_ab maps the caller's raw fp32 A (K x M extents, zero fill outside)
   // and the kernel splits it into tf32 big/small in shared memory; tmap_as is

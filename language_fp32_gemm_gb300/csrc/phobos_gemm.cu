@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -62,7 +63,61 @@ int tc_kind(int path) {
 }
 // Tail split: at most this many K pieces per tile, each at least this many K blocks.
 constexpr int kMaxTailSplit = 8;
-constexpr int kMinPieceBlocks = 4;
+// Workers (CTAs or CTA pairs) that share the `tail` tiles of the last, partial
+// wave, each taking an even share of the tail's K blocks (0 = no split).
+// split: the plan's tail_split (0 = automatic, 1 = off, S = S pieces per tile
+// when S workers per tail tile are free, else an even share for every worker).
+// S is capped so that a share spans at least kMinPieceBlocks.  With more
+// workers than tail tiles a share is shorter than a tile; moving its ends onto
+// tile boundaries (the kernel does that for pieces shorter than
+// kMinPieceBlocks) lengthens it by less than 2 * kMinPieceBlocks <= one tile,
+// so a share never reaches into a third tile.
+int tail_workers(int split, int tail, int units, int k_blocks) {
+  if (split == 1 || tail == 0) return 0;
+  // Automatic: S pieces per tile shorten the tail from k_blocks to about
+  // k_blocks / S blocks of MMA work, and each piece after the first costs its
+  // owner about 2.5 blocks' time to add (1.6 to 2.3 us measured on GB300, a
+  // block being 0.8 us); k_blocks / S + 2.5 * (S - 1) is least at
+  // S = sqrt(k_blocks / 2.5).
+  int S = split;
+  if (split == 0) {
+    S = static_cast<int>(std::lround(std::sqrt(k_blocks / 2.5)));
+    if (S > kMaxTailSplit) S = kMaxTailSplit;
+  }
+  if (S > k_blocks / kMinPieceBlocks) S = k_blocks / kMinPieceBlocks;
+  if (S < 2) return 0;
+  int64_t w = static_cast<int64_t>(tail) * S < units ? static_cast<int64_t>(tail) * S : units;
+  if (w > kMaxTailUnits) w = kMaxTailUnits;
+  return w > tail ? static_cast<int>(w) : 0;
+}
+
+// Worker w's share of the tail starts at K block floor(w * T / tail_units) of
+// the T = tail * k_blocks blocks of the tail tiles laid end to end; a start
+// closer than kMinPieceBlocks to a tile boundary moves onto it (a monotone
+// map, so shares stay ordered).  Every piece then spans at least
+// kMinPieceBlocks, or a whole tile.  Two starts can land on the same boundary
+// when shares are short; the kernel wants no empty share (the later pieces of
+// a tile are then consecutive workers), so fewer workers are used until none
+// is empty.  Returns the number of workers (0 = no split).
+int fill_tail_shares(TcArgs &t, int tail, int workers) {
+  const int64_t kb = t.k_blocks, total = static_cast<int64_t>(tail) * kb;
+  for (; workers > tail; --workers) {
+    bool empty = false;
+    for (int w = 0; w <= workers; ++w) {
+      int64_t s = total * w / workers;
+      const int64_t r = s % kb;
+      if (r != 0 && r < kMinPieceBlocks) s -= r;
+      else if (r != 0 && kb - r < kMinPieceBlocks) s += kb - r;
+      t.tail_tile[w] = static_cast<int>(s / kb);
+      t.tail_k[w] = static_cast<int>(s % kb);
+      if (w > 0 && t.tail_tile[w] == t.tail_tile[w - 1] && t.tail_k[w] == t.tail_k[w - 1])
+        empty = true;
+    }
+    if (!empty) return workers;
+  }
+  return 0;
+}
+
 constexpr int kEpiWarps = 8;  // accumulator warps of the tensor-core kernel (one flag each)
 // Automatic a_split: split A inside the kernel up to this N.  A pre-pass over
 // A costs about 6 * (TF32/3 rate) / (N * HBM bandwidth) of the GEMM time,
@@ -431,25 +486,16 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   // workspace: [B big][B small][A big][A small] (no A part when A is split in-kernel)
   const size_t ops_bytes = static_cast<size_t>(ops * b_bytes + (a_inline ? 0 : ops * a_bytes));
 
-  // Persistent grid: one CTA (pair) per SM (pair).  Split the tiles of the
-  // last, partial wave along K so that idle SMs share the tail.
+  // Persistent grid: one CTA (pair) per SM (pair).  The tiles of the last,
+  // partial wave are split along K so that idle SMs share the tail.
   const int units = pair ? dev.sm_count / 2 : dev.sm_count;
   const int total_tiles = static_cast<int>((Mp / bm) * (Np / bn));
   const int chunk_blocks_max =
       static_cast<int>(round_up(p.super_k < K ? p.super_k : K, bk) / bk);
-  int tail_split = 1, full_tiles = total_tiles;
   const int tail = units > 0 ? total_tiles % units : 0;
-  if (p.tail_split != 1 && tail != 0) {
-    int S = p.tail_split >= 2 ? p.tail_split : units / tail;
-    if (S > kMaxTailSplit) S = kMaxTailSplit;
-    if (S > chunk_blocks_max / kMinPieceBlocks) S = chunk_blocks_max / kMinPieceBlocks;
-    if (S * tail > units) S = units / tail;
-    if (S >= 2) {
-      tail_split = S;
-      full_tiles = total_tiles - tail;
-    }
-  }
-  const int64_t slots = tail_split > 1 ? static_cast<int64_t>(tail) * (tail_split - 1) : 0;
+  const int tail_units = tail_workers(p.tail_split, tail, units, chunk_blocks_max);
+  const int full_tiles = tail_units > 0 ? total_tiles - tail : total_tiles;
+  const int64_t slots = tail_units;  // one partial sum per worker at most
   const size_t part_bytes = static_cast<size_t>(round_up(slots * bm * bn * 4, 256));
   const size_t flag_bytes = static_cast<size_t>(round_up(slots * 2 * kEpiWarps * 4, 256));
   const size_t need = ops_bytes + part_bytes + flag_bytes;
@@ -534,10 +580,10 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   t.sm_count = dev.sm_count;
   t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD") ? 1 : 0;
   t.full_tiles = full_tiles;
-  t.tail_split = tail_split;
-  // every K piece of the tail needs its own CTA (pair); whole tiles stride over
-  // all SMs (pairs)
-  t.grid_units = tail_split > 1 ? (full_tiles > 0 ? units : tail * tail_split)
+  t.tail_units = tail_units;
+  // whole tiles stride over all SMs (pairs); with no whole tiles, only the
+  // workers sharing the tail are launched
+  t.grid_units = tail_units > 0 ? (full_tiles > 0 ? units : tail_units)
                                 : (total_tiles < units ? total_tiles : units);
   t.partials = partials;
   t.flags = flags;
@@ -549,6 +595,10 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     t.beta = beta;
     t.k_block0 = 0;
     t.k_blocks = total_blocks;
+    if (t.tail_units > 0) {
+      t.tail_units = fill_tail_shares(t, tail, t.tail_units);
+      if (t.tail_units == 0) t.full_tiles = total_tiles;
+    }
     if (mark(g_ev_start, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
     st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream, kind)
                                    : launch_tc(t, passes, bn, p.stages, stream, kind)));
@@ -565,9 +615,11 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     t.k_block0 = kb;
     t.k_blocks = total_blocks - kb < chunk_blocks ? total_blocks - kb : chunk_blocks;
     // a short last chunk may not afford as many pieces
-    if (t.tail_split > 1 && t.tail_split > t.k_blocks / kMinPieceBlocks) {
-      t.tail_split = t.k_blocks / kMinPieceBlocks >= 2 ? t.k_blocks / kMinPieceBlocks : 1;
-      if (t.tail_split == 1) t.full_tiles = total_tiles;
+    if (t.tail_units > 0) {
+      int w = tail_workers(p.tail_split, tail, units, t.k_blocks);
+      if (w > tail_units) w = tail_units;  // the slots sized above
+      t.tail_units = w > 0 ? fill_tail_shares(t, tail, w) : 0;
+      if (t.tail_units == 0) t.full_tiles = total_tiles;
     }
     st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream, kind)
                                    : launch_tc(t, passes, bn, p.stages, stream, kind)));

@@ -108,18 +108,24 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
   tn = r / rows;
 }
 
-// One unit of work of a persistent CTA (pair): a whole tile, or one K piece of
-// a tile of the last wave (piece >= 0).
+// One unit of work of a persistent CTA (pair): a whole tile (piece = -1), or
+// one K piece of a tail tile: piece 0 starts at k = 0 and owns the tile (it
+// adds the other pieces and stores C), piece 1 is any later piece (its sum goes
+// to partials slot `worker`).
 struct Unit {
   int tile, k_lo, k_hi, piece;
 };
 
 // The i-th unit of worker w out of `units`: whole tiles w, w + units, ... below
-// full_tiles, then at most one K piece of a tail tile.  Every role of the CTA
-// walks the same sequence.
+// full_tiles, then the pieces of its share of the tail (the host deals the
+// tail's K blocks to tail_units workers): at most two, since a share is shorter
+// than a tile (the end of one tail tile, then the start of the next).  A later
+// piece is always the first piece of its worker, so it never waits on
+// anything; only piece 0 waits, for later pieces, which every worker reaches
+// right after its whole tiles.  Every role of the CTA walks the same sequence.
 __device__ __forceinline__ bool unit_of(const TcArgs &p, int w, int units, int i, Unit &u) {
   const int total = p.tiles_m * p.tiles_n;
-  if (p.tail_split <= 1) {
+  if (p.tail_units <= 0) {
     const int t = w + i * units;
     if (t >= total) return false;
     u = Unit{t, 0, p.k_blocks, -1};
@@ -130,13 +136,20 @@ __device__ __forceinline__ bool unit_of(const TcArgs &p, int w, int units, int i
     u = Unit{w + i * units, 0, p.k_blocks, -1};
     return true;
   }
-  const int S = p.tail_split;
-  if (i > n_whole || w >= (total - p.full_tiles) * S) return false;
-  const int piece = w % S;
-  u.tile = p.full_tiles + w / S;
-  u.piece = piece;
-  u.k_lo = static_cast<int>(static_cast<long long>(p.k_blocks) * piece / S);
-  u.k_hi = static_cast<int>(static_cast<long long>(p.k_blocks) * (piece + 1) / S);
+  const int j = i - n_whole;
+  if (w >= p.tail_units || j > 1) return false;
+  const int st = p.tail_tile[w], sk = p.tail_k[w];
+  const int et = p.tail_tile[w + 1], ek = p.tail_k[w + 1];
+  if (st > et || (st == et && sk >= ek)) return false;  // an empty share
+  if (j == 0) {
+    u.tile = p.full_tiles + st;
+    u.k_lo = sk;
+    u.k_hi = et > st ? p.k_blocks : ek;
+    u.piece = sk == 0 ? 0 : 1;
+    return true;
+  }
+  if (et != st + 1 || ek == 0) return false;  // the share ends inside (or at the end of) its first tile
+  u = Unit{p.full_tiles + st + 1, 0, ek, 0};
   return true;
 }
 
@@ -648,10 +661,10 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       // layout: float4 v of lane l of a warp sits at (v * 32 + l), so that every
       // store and load instruction covers 512 contiguous bytes.
       if (u.piece > 0) {
-        // Hand the partial sum to the piece-0 owner, then release the flag once
-        // every accumulator thread's stores are visible.
-        const long long slot = static_cast<long long>(u.tile - p.full_tiles) * (p.tail_split - 1) +
-                               (u.piece - 1);
+        // Hand the partial sum to the piece-0 owner through this worker's
+        // slot, then release the flag once every accumulator thread's stores
+        // are visible.
+        const long long slot = unit;
         float4 *dst = reinterpret_cast<float4 *>(p.partials) +
                       ((slot * kRanks + rank) * kEpiWarps + (warp - 2)) * (kHalf / 4) * 32 + lane;
 #pragma unroll
@@ -666,11 +679,14 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         continue;
       }
       if (u.piece == 0) {
-        // Owner: add the other pieces in piece order (deterministic).
-        for (int pc = 1; pc < p.tail_split && ok; ++pc) {
-          const long long slot =
-              static_cast<long long>(u.tile - p.full_tiles) * (p.tail_split - 1) + (pc - 1);
-          const unsigned *flag = p.flags + (slot * 2 + rank) * kEpiWarps + (warp - 2);
+        // Owner: add the later pieces of this tile in K order (deterministic).
+        // They are the first pieces of the next workers, w_end excluded: the
+        // host leaves no share empty, so these are consecutive.
+        const int tt = u.tile - p.full_tiles;
+        int w_end = unit + 1;
+        while (w_end < p.tail_units && p.tail_tile[w_end] == tt) ++w_end;
+        for (int w2 = unit + 1; w2 < w_end && ok; ++w2) {
+          const unsigned *flag = p.flags + (static_cast<long long>(w2) * 2 + rank) * kEpiWarps + (warp - 2);
           if (ld_acquire_gpu(flag) != p.epoch) {
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t polls = 1; ld_acquire_gpu(flag) != p.epoch; ++polls) {
@@ -684,23 +700,65 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
               }
             }
           }
-          if (!ok) break;
-          const float4 *src = reinterpret_cast<const float4 *>(p.partials) +
-                              ((slot * kRanks + rank) * kEpiWarps + (warp - 2)) * (kHalf / 4) * 32 +
-                              lane;
-#pragma unroll
-          for (int v = 0; v < kHalf / 4; ++v) {
-            const float4 x = __ldcg(src + v * 32);
-            sum[4 * v + 0] = __fadd_rn(sum[4 * v + 0], x.x);
-            sum[4 * v + 1] = __fadd_rn(sum[4 * v + 1], x.y);
-            sum[4 * v + 2] = __fadd_rn(sum[4 * v + 2], x.z);
-            sum[4 * v + 3] = __fadd_rn(sum[4 * v + 3], x.w);
-          }
         }
         if (!ok) {
           cp_async_wait_all();
           break;
         }
+        // The pieces stream through the operand ring, which is idle now: an
+        // owner piece is its worker's last unit, and its final partial sum
+        // landed after every MMA of the worker had read its operands.  Each
+        // lane copies and later reads only its own float4s, so no warp
+        // barrier is needed; kBufs - 1 chunks are in flight while one is added
+        // (registers alone held too few loads in flight: 3 to 5 us per piece).
+        constexpr int kChunkF4 = 4;                     // float4 per lane per chunk
+        constexpr int kSlotF4 = kHalf / 4;              // float4 per lane per piece
+        constexpr int kCps = kSlotF4 / kChunkF4;        // chunks per piece
+        constexpr int kRingF4PerWarp = STAGES * S::kStageBytes / 16 / kEpiWarps;
+        constexpr int kBufs0 = kRingF4PerWarp / (32 * kChunkF4);
+        // a power of two, at most 8
+        constexpr int kBufs = kBufs0 >= 8 ? 8 : kBufs0 >= 4 ? 4 : kBufs0 >= 2 ? 2 : 0;
+        static_assert(kBufs >= 2 && kSlotF4 % kChunkF4 == 0, "fix-up staging fits the ring");
+        const uint32_t stage = tiles + ((warp - 2) * (kBufs * kChunkF4 * 32) + lane) * 16u;
+        const float4 *part0 = reinterpret_cast<const float4 *>(p.partials) +
+                              ((static_cast<long long>(unit + 1) * kRanks + rank) * kEpiWarps + (warp - 2)) *
+                                  (kSlotF4 * 32) + lane;
+        // the pieces' slots are consecutive: piece i of this warp at part0 + i * kSlotStride
+        constexpr long long kSlotStride = static_cast<long long>(kRanks) * kEpiWarps * kSlotF4 * 32;
+        const int n_chunks = (w_end - unit - 1) * kCps;
+        auto issue = [&](int c) {
+          if (c < n_chunks) {
+            const float4 *src = part0 + (c / kCps) * kSlotStride + (c % kCps) * (kChunkF4 * 32);
+            const uint32_t dst = stage + (c % kBufs) * (kChunkF4 * 32 * 16);
+#pragma unroll
+            for (int q = 0; q < kChunkF4; ++q) cp_async16_u32(dst + q * 32 * 16, src + q * 32);
+          }
+          cp_async_commit();  // an empty group past the end keeps the count
+        };
+        if (n_chunks > 0) {
+#pragma unroll 1
+          for (int c = 0; c < kBufs - 1; ++c) issue(c);
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < n_chunks; c0 += kCps) {
+#pragma unroll
+          for (int j = 0; j < kCps; ++j) {
+            const int c = c0 + j;
+            issue(c + kBufs - 1);  // into the buffer of chunk c - 1, added already
+            cp_async_wait_group<kBufs - 1>();  // chunk c has landed
+            const uint32_t b = stage + (c % kBufs) * (kChunkF4 * 32 * 16);
+#pragma unroll
+            for (int q = 0; q < kChunkF4; ++q) {
+              const float4 x = ld_shared_f4(b + q * 32 * 16);
+              const int v = j * kChunkF4 + q;
+              sum[4 * v + 0] = __fadd_rn(sum[4 * v + 0], x.x);
+              sum[4 * v + 1] = __fadd_rn(sum[4 * v + 1], x.y);
+              sum[4 * v + 2] = __fadd_rn(sum[4 * v + 2], x.z);
+              sum[4 * v + 3] = __fadd_rn(sum[4 * v + 3], x.w);
+            }
+          }
+        }
+        cp_async_wait_all();
       }
       if (!writes_c) continue;
       // The tile's sum is in registers: TMEM already serves the next tile's
