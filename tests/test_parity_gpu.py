@@ -316,3 +316,35 @@ def test_split_tf32_short_k_stress(dev, K):
     A = si.normal(97, 0, (M, K))
     B = si.normal(97, 1, (K, N))
     check(dev, A, B, np.zeros((M, N), np.float32), 1.0, 0.0, "3xtf32")
+
+
+# ------------------------------- inputs of one sign: the bound's other side
+
+@pytest.mark.parametrize("K", [256, 1024, 4096])
+@pytest.mark.parametrize("math", ["3xtf32", "ffma"])
+def test_same_sign_inputs_within_their_accumulation_bound(dev, math, K):
+    # The 2^-20 bound holds for zero-mean data, as in every workload.  When all
+    # products share a sign, the running sum grows like sum|a||b| and every
+    # fp32 addition rounds relative to it, so no fp32 accumulation meets 2^-20
+    # at large K (measured on GB300: FFMA 4.2e-6, split TF32 2.6e-6 at
+    # K = 4096).  Each path must still stay inside the worst case of its own
+    # arithmetic, which a missing promotion (8.6e-5 at K = 8192) or a dropped
+    # split pass (about 2^-11) would break:
+    #  - FFMA: K additions, each rounded to nearest (2^-24 of the running sum);
+    #  - split TF32: a TMEM partial holds at most 8 K blocks, 96 tensor-core
+    #    updates, each truncating within one ulp (2^-23) of the running sum,
+    #    allowed one more ulp for the tensor core's own sum of its 8 products;
+    #    at most one rounded register addition per K block (2^-24 each); the
+    #    split drops a_small*b_small and rounds the small parts (3 * 2^-22).
+    M, N = 512, 1024
+    A = np.abs(si.uniform_pm1(98, 0, (M, K)))
+    B = np.abs(si.uniform_pm1(98, 1, (K, N)))
+    C0 = np.zeros((M, N), np.float32)
+    C = run_gemm(torch, dev, A, B, C0, 1.0, 0.0, math)
+    ref, den = oracle.sgemm(A, B, C0, 1.0, 0.0)
+    err = oracle.max_rel_error(C, ref, den)
+    if math == "ffma":
+        bound = K * 2.0 ** -24
+    else:
+        bound = 96 * 2.0 ** -22 + (K / 32 + 1) * 2.0 ** -24 + 3 * 2.0 ** -22
+    assert err <= bound, "max rel error %.3g > %.3g" % (err, bound)
