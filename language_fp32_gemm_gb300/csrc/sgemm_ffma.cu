@@ -158,6 +158,9 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 1)
 
   if (KSPLIT) {
     // Cluster reduction of the K slices through distributed shared memory.
+    // Every rank reduces its own share of the tile's rows: it reads that
+    // share from every rank's partial tile (its own included), adds the
+    // slices in rank order (deterministic), and stores those rows of C.
     __shared__ __align__(16) float part[BM * BN];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -168,60 +171,113 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 1)
             make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
     }
     cluster_sync();  // every slice's partial tile is in place
-    if (slice == 0) {
-      for (int rk = 1; rk < p.kslices; ++rk) {
+    const int rows_per = (BM + p.kslices - 1) / p.kslices;
+    const int r_lo = slice * rows_per;
+    const int r_hi = min(BM, r_lo + rows_per);
+    constexpr int kVecPerRow = BN / 4;
+#pragma unroll 1
+    for (int e = r_lo * kVecPerRow + tid; e < r_hi * kVecPerRow; e += NT) {
+      const int r = e / kVecPerRow, c = (e - r * kVecPerRow) * 4;
+      const uint32_t local = smem_u32(&part[r * BN + c]);
+      float4 v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4);
+      for (int rk = 0; rk < 8; ++rk)
+        if (rk < p.kslices) v[rk] = ld_shared_cluster_v4(mapa_shared(local, rk));
+      float4 t = v[0];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t addr =
-                mapa_shared(smem_u32(&part[r * BN + tx * 4 + h * (BN / 2)]), rk);
-            const float4 v = ld_shared_cluster_v4(addr);
-            acc[i][4 * h + 0] += v.x;
-            acc[i][4 * h + 1] += v.y;
-            acc[i][4 * h + 2] += v.z;
-            acc[i][4 * h + 3] += v.w;
+      for (int rk = 1; rk < 8; ++rk)
+        if (rk < p.kslices) {
+          t.x += v[rk].x;
+          t.y += v[rk].y;
+          t.z += v[rk].z;
+          t.w += v[rk].w;
+        }
+      const int row = m0 + r, col = n0 + c;
+      if (row < p.M) {
+        float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+        const float tv[4] = {t.x, t.y, t.z, t.w};
+        if (p.vec_c && col + 3 < p.N) {
+          float4 *dst = reinterpret_cast<float4 *>(crow + col);
+          float4 o;
+          if (p.beta != 0.0f) {
+            const float4 old = *dst;
+            o.x = fmaf(p.alpha, tv[0], p.beta * old.x);
+            o.y = fmaf(p.alpha, tv[1], p.beta * old.y);
+            o.z = fmaf(p.alpha, tv[2], p.beta * old.z);
+            o.w = fmaf(p.alpha, tv[3], p.beta * old.w);
+          } else {
+            o.x = p.alpha * tv[0];
+            o.y = p.alpha * tv[1];
+            o.z = p.alpha * tv[2];
+            o.w = p.alpha * tv[3];
           }
+          *dst = o;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (col + q < p.N)
+              crow[col + q] = p.beta != 0.0f ? fmaf(p.alpha, tv[q], p.beta * crow[col + q])
+                                             : p.alpha * tv[q];
         }
       }
     }
-    cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
-    if (slice != 0) return;
+    cluster_sync();  // the peers' shared memory stays valid until every rank has read it
+    return;
   }
 
   // Epilogue: C = alpha * acc + beta * C_old; beta == 0 does not read C.
+  // Old C of all the thread's rows is loaded before any store: a store could
+  // alias a later load as far as the compiler knows, which would otherwise
+  // serialise one memory round trip per row.  The 128-row tile (two CTAs per
+  // SM, fewer registers) does it half a micro-tile at a time.
+  constexpr int kHalfRows = BM == 128 ? 4 : 8;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
-    if (row >= p.M) continue;
-    float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+  for (int i0 = 0; i0 < 8; i0 += kHalfRows) {
+    float4 old[kHalfRows][2];
+    if (p.beta != 0.0f) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int col = n0 + tx * 4 + h * (BN / 2);
-      if (p.vec_c && col + 3 < p.N) {
-        float4 *dst = reinterpret_cast<float4 *>(crow + col);
-        float4 o;
-        if (p.beta != 0.0f) {
-          const float4 old = *dst;
-          o.x = fmaf(p.alpha, acc[i][4 * h + 0], p.beta * old.x);
-          o.y = fmaf(p.alpha, acc[i][4 * h + 1], p.beta * old.y);
-          o.z = fmaf(p.alpha, acc[i][4 * h + 2], p.beta * old.z);
-          o.w = fmaf(p.alpha, acc[i][4 * h + 3], p.beta * old.w);
-        } else {
-          o.x = p.alpha * acc[i][4 * h + 0];
-          o.y = p.alpha * acc[i][4 * h + 1];
-          o.z = p.alpha * acc[i][4 * h + 2];
-          o.w = p.alpha * acc[i][4 * h + 3];
-        }
-        *dst = o;
-      } else {
+      for (int i = i0; i < i0 + kHalfRows; ++i) {
+        const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+        const float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (col + t < p.N) {
-            const float v = acc[i][4 * h + t];
-            crow[col + t] = p.beta != 0.0f ? fmaf(p.alpha, v, p.beta * crow[col + t]) : p.alpha * v;
+        for (int h = 0; h < 2; ++h) {
+          const int col = n0 + tx * 4 + h * (BN / 2);
+          float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row < p.M) {
+            if (p.vec_c && col + 3 < p.N) {
+              o = *reinterpret_cast<const float4 *>(crow + col);
+            } else {
+              if (col + 0 < p.N) o.x = crow[col + 0];
+              if (col + 1 < p.N) o.y = crow[col + 1];
+              if (col + 2 < p.N) o.z = crow[col + 2];
+              if (col + 3 < p.N) o.w = crow[col + 3];
+            }
           }
+          old[i - i0][h] = o;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = i0; i < i0 + kHalfRows; ++i) {
+      const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+      if (row >= p.M) continue;
+      float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int col = n0 + tx * 4 + h * (BN / 2);
+        const float4 od = old[i - i0][h];
+        const float oldv[4] = {od.x, od.y, od.z, od.w};
+        float o[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          o[t] = p.beta != 0.0f ? fmaf(p.alpha, acc[i][4 * h + t], p.beta * oldv[t])
+                                : p.alpha * acc[i][4 * h + t];
+        if (p.vec_c && col + 3 < p.N) {
+          *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (col + t < p.N) crow[col + t] = o[t];
         }
       }
     }
