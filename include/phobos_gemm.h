@@ -111,14 +111,15 @@ typedef enum {
  *  tail_split      FFMA path with 64 x 64 tiles: K slices per tile, summed
  *                  inside a thread-block cluster through distributed shared
  *                  memory (0 = enough to fill the SMs, 1 = off, 2..8).
- *                  Tensor-core paths: the K blocks of the tiles of the last,
- *                  partial wave of the persistent grid are dealt evenly to
- *                  the CTAs (pairs) that would otherwise idle, so the tail
- *                  ends at the same time everywhere (0 = every SM pair, up to
- *                  8 per tail tile; 1 = off; S = 2..8 = at most S per tail
- *                  tile: S equal pieces per tile when that many are free).
- *                  Every piece spans at least K = 128.  Results are equal up
- *                  to rounding order and deterministic.
+ *                  Tensor-core paths: each tile of the last, partial wave of
+ *                  the persistent grid is cut along K into pieces for the
+ *                  CTAs (pairs) that would otherwise idle (0 = automatic:
+ *                  about sqrt(K / 80) pieces, as many as the idle CTAs
+ *                  allow, at most 8; 1 = off; S = 2..8: S pieces per tile,
+ *                  or, when fewer than S CTAs per tail tile are free, the
+ *                  tail's K blocks dealt evenly to every CTA).  Every piece
+ *                  spans at least K = 128.  Results are equal up to rounding
+ *                  order and deterministic.
  *  a_split         tensor-core paths: where A is split into tf32 big/small
  *                  (0 = chosen per call: inside the kernel when N <= 1536 and
  *                  A's rows are 16-byte aligned, where a separate pass over A

@@ -74,15 +74,20 @@ constexpr int kMaxTailSplit = 8;
 // so a share never reaches into a third tile.
 int tail_workers(int split, int tail, int units, int k_blocks) {
   if (split == 1 || tail == 0) return 0;
-  // Automatic: S pieces per tile shorten the tail from k_blocks to about
-  // k_blocks / S blocks of MMA work, and each piece after the first costs its
-  // owner about 2.5 blocks' time to add (1.6 to 2.3 us measured on GB300, a
-  // block being 0.8 us); k_blocks / S + 2.5 * (S - 1) is least at
-  // S = sqrt(k_blocks / 2.5).
   int S = split;
   if (split == 0) {
+    // S pieces per tile shorten the tail from k_blocks to about k_blocks / S
+    // blocks of MMA work, and each piece after the first costs its owner about
+    // 2.5 blocks' time to add (1.6 to 2.3 us measured on GB300, a block being
+    // 0.8 us): k_blocks / S + 2.5 * (S - 1) is least at S = sqrt(k_blocks / 2.5).
     S = static_cast<int>(std::lround(std::sqrt(k_blocks / 2.5)));
     if (S > kMaxTailSplit) S = kMaxTailSplit;
+    // Whole pieces only: every tail tile is then cut at the same K offsets, so
+    // tiles that share an A or B panel read it at the same time, as whole
+    // tiles do.  Even shares across tile boundaries put concurrent pieces at
+    // different K offsets: on a 1024 x 8192 x 8192 band the tail then read its
+    // B panels from DRAM again and the kernel took 500 us instead of 438 us.
+    if (S > units / tail) S = units / tail;
   }
   if (S > k_blocks / kMinPieceBlocks) S = k_blocks / kMinPieceBlocks;
   if (S < 2) return 0;
