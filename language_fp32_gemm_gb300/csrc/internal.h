@@ -37,6 +37,24 @@ cudaError_t launch_split_rows(const float *A, int64_t lda, int M, int K, int Mp,
 // B (K x N, row-major, ldb) -> transposed big/small [Np][Kp] (K-major); zero padding.
 cudaError_t launch_split_cols(const float *B, int64_t ldb, int K, int N, int Np, int Kp,
                               float *big, float *small, cudaStream_t stream);
+// Both splits and the zeroing of the tail-split flags in one launch.  The
+// launcher fills a_blocks and b_tiles_*; split_a / split_b select the parts
+// (a launch with neither only zeroes the flags).
+struct SplitArgs {
+  const float *A;
+  int64_t lda;
+  int M, K, Mp, Kp;
+  float *a_big, *a_small;  // a_small may be null (one-pass TF32)
+  int vec_a;               // 16-byte loads of A allowed
+  const float *B;
+  int64_t ldb;
+  int N, Np;
+  float *b_big, *b_small;  // b_small may be null
+  unsigned *flags;
+  int64_t n_flags;
+  int a_blocks, b_tiles_k, b_tiles_n;
+};
+cudaError_t launch_split_ab(SplitArgs a, int split_a, int split_b, cudaStream_t stream);
 // The same layouts with one 16-bit operand (fp16 when bf16 == 0, else bf16),
 // each element rounded to nearest, ties to even.  `out` holds 2-byte elements.
 cudaError_t launch_convert_rows(const float *A, int64_t lda, int M, int K, int Mp, int Kp,

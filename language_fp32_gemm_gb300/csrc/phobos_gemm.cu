@@ -512,9 +512,6 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   float *partials = reinterpret_cast<float *>(static_cast<char *>(ws.ptr) + ops_bytes);
   unsigned *flags =
       reinterpret_cast<unsigned *>(static_cast<char *>(ws.ptr) + ops_bytes + part_bytes);
-  // Flags must not hold a value a launch of this call will wait for.
-  if (flag_bytes && cudaMemsetAsync(flags, 0, flag_bytes, stream) != cudaSuccess)
-    return PHOBOS_ERR_CUDA;
   if ((st = get_encoder()) != PHOBOS_OK) return st;
 
   char *base = static_cast<char *>(ws.ptr);
@@ -523,7 +520,11 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   float *a_big = reinterpret_cast<float *>(base + ops * b_bytes);
   float *a_small = passes == 3 ? reinterpret_cast<float *>(base + ops * b_bytes + a_bytes) : nullptr;
 
+  // Flags must not hold a value a launch of this call will wait for: the
+  // split-TF32 / TF32 pre-pass zeroes them in the same launch.
   if (half) {
+    if (flag_bytes && cudaMemsetAsync(flags, 0, flag_bytes, stream) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
     st = cuda_status(counted(launch_convert_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
                                                  static_cast<int>(Mp), static_cast<int>(Kp), a_big,
                                                  kind == kTcBf16, stream)));
@@ -534,19 +535,27 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
                                                    kind == kTcBf16, stream)));
       if (st != PHOBOS_OK) return st;
     }
-  } else {
-    if (!a_inline) {
-      st = cuda_status(counted(launch_split_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
-                                                 static_cast<int>(Mp), static_cast<int>(Kp), a_big,
-                                                 a_small, a_tma_ok, stream)));
-      if (st != PHOBOS_OK) return st;
-    }
-    if (!reuse_b) {
-      st = cuda_status(counted(launch_split_cols(B, ldb, static_cast<int>(K), static_cast<int>(N),
-                                                 static_cast<int>(Np), static_cast<int>(Kp), b_big,
-                                                 b_small, stream)));
-      if (st != PHOBOS_OK) return st;
-    }
+  } else if (!a_inline || !reuse_b || flag_bytes) {
+    SplitArgs sa{};
+    sa.A = A;
+    sa.lda = lda;
+    sa.M = static_cast<int>(M);
+    sa.K = static_cast<int>(K);
+    sa.Mp = static_cast<int>(Mp);
+    sa.Kp = static_cast<int>(Kp);
+    sa.a_big = a_big;
+    sa.a_small = a_small;
+    sa.vec_a = a_tma_ok ? 1 : 0;
+    sa.B = B;
+    sa.ldb = ldb;
+    sa.N = static_cast<int>(N);
+    sa.Np = static_cast<int>(Np);
+    sa.b_big = b_big;
+    sa.b_small = b_small;
+    sa.flags = flags;
+    sa.n_flags = static_cast<int64_t>(flag_bytes / 4);
+    st = cuda_status(counted(launch_split_ab(sa, a_inline ? 0 : 1, reuse_b ? 0 : 1, stream)));
+    if (st != PHOBOS_OK) return st;
   }
 
   TcArgs t{};

@@ -86,6 +86,72 @@ __global__ void __launch_bounds__(256) split_cols_kernel(const float *__restrict
   }
 }
 
+// The whole split-TF32 pre-pass in one launch: blocks [0, a_blocks) split A
+// row by row (a grid-stride loop over A's float4 groups, as split_rows_kernel),
+// the next b_tiles_k * b_tiles_n blocks each split and transpose one 32 x 32
+// tile of B (as split_cols_kernel), and every thread also zeroes its share of
+// the tail-split flags.  One launch instead of a flag memset and two kernels
+// saves their launch gaps on the stream.
+__global__ void __launch_bounds__(256) split_ab_kernel(const SplitArgs a) {
+  __shared__ float tile[32][33];
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < a.n_flags;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    a.flags[i] = 0u;
+  if (static_cast<int>(blockIdx.x) < a.a_blocks) {
+    const int64_t groups_per_row = a.Kp / 4;
+    const int64_t total = static_cast<int64_t>(a.Mp) * groups_per_row;
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+         g += static_cast<int64_t>(a.a_blocks) * blockDim.x) {
+      const int i = static_cast<int>(g / groups_per_row);
+      const int k = static_cast<int>(g - static_cast<int64_t>(i) * groups_per_row) * 4;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (i < a.M) {
+        const float *src = a.A + static_cast<int64_t>(i) * a.lda + k;
+        if (a.vec_a && k + 3 < a.K) {
+          const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+          x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (k + t < a.K) x[t] = __ldg(src + t);
+        }
+      }
+      float4 b, s;
+      b.x = tf32_rna_bits(x[0]); s.x = tf32_rna_bits(x[0] - b.x);
+      b.y = tf32_rna_bits(x[1]); s.y = tf32_rna_bits(x[1] - b.y);
+      b.z = tf32_rna_bits(x[2]); s.z = tf32_rna_bits(x[2] - b.z);
+      b.w = tf32_rna_bits(x[3]); s.w = tf32_rna_bits(x[3] - b.w);
+      const int64_t o = static_cast<int64_t>(i) * a.Kp + k;
+      *reinterpret_cast<float4 *>(a.a_big + o) = b;
+      if (a.a_small) *reinterpret_cast<float4 *>(a.a_small + o) = s;
+    }
+    return;
+  }
+  const int t = static_cast<int>(blockIdx.x) - a.a_blocks;
+  if (t >= a.b_tiles_k * a.b_tiles_n) return;
+  const int k0 = (t % a.b_tiles_k) * 32;
+  const int n0 = (t / a.b_tiles_k) * 32;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;  // 0..7
+#pragma unroll
+  for (int r = 0; r < 32; r += 8) {
+    const int k = k0 + ty + r;
+    const int n = n0 + tx;
+    tile[ty + r][tx] = (k < a.K && n < a.N) ? __ldg(a.B + static_cast<int64_t>(k) * a.ldb + n) : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 32; r += 8) {
+    const int n = n0 + ty + r;
+    const int k = k0 + tx;
+    const float x = tile[tx][ty + r];
+    const float b = tf32_rna_bits(x);
+    const int64_t o = static_cast<int64_t>(n) * a.Kp + k;
+    a.b_big[o] = b;
+    if (a.b_small) a.b_small[o] = tf32_rna_bits(x - b);
+  }
+}
+
 template <bool BF16>
 __device__ __forceinline__ unsigned short to_16bit(float x) {
   if (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -181,6 +247,19 @@ cudaError_t launch_split_cols(const float *B, int64_t ldb, int K, int N, int Np,
                               float *big, float *small, cudaStream_t stream) {
   dim3 grid(Kp / 32, Np / 32);
   split_cols_kernel<<<grid, 256, 0, stream>>>(B, ldb, K, N, Kp, big, small);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_ab(SplitArgs a, int split_a, int split_b, cudaStream_t stream) {
+  a.a_blocks = split_a ? static_cast<int>(grid_for(static_cast<int64_t>(a.Mp) * (a.Kp / 4), 256)) : 0;
+  a.b_tiles_k = split_b ? a.Kp / 32 : 0;
+  a.b_tiles_n = split_b ? a.Np / 32 : 0;
+  const int64_t blocks = a.a_blocks + static_cast<int64_t>(a.b_tiles_k) * a.b_tiles_n;
+  const int64_t flag_blocks = (a.n_flags + 255) / 256;
+  const int64_t grid = blocks > flag_blocks ? blocks : flag_blocks;
+  if (grid == 0) return cudaSuccess;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  split_ab_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
