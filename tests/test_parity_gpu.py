@@ -215,6 +215,10 @@ def test_timing_events_and_launch_count(dev):
     ((1000, 100, 1024), 0, None),    # single-CTA tiles (N <= 128)
     ((520, 390, 2100), 0, 512),      # split inside every K chunk of the cluster split
     ((777, 1290, 333), 0, None),     # ragged edges, short K: pieces of at least 4 blocks
+    # 100 pair tiles: 24 tail tiles; 8 pieces each would need 192 pairs, so the
+    # tail's K blocks are dealt evenly to all of them (shares across tiles)
+    ((2560, 2560, 2048), 8, None),
+    ((2500, 2510, 1100), 8, 512),    # the same inside K chunks, ragged edges
 ], ids=lambda v: str(v))
 def test_tail_split(dev, math, shape, split, super_k):
     M, N, K = shape
