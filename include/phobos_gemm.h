@@ -96,9 +96,18 @@ typedef enum {
  *  tile_k          K depth of one shared-memory stage: 16 for FFMA, 32 for
  *                  the tf32 paths, 64 for FP16 and BF16 (128 bytes of K
  *                  either way on the tensor cores).
- *  cluster_m/_n    CTAs per thread-block cluster along M and N (1 x 1 or 2 x 1).
+ *  cluster_m/_n    CTAs per thread-block cluster along M and N: 1 x 1, 2 x 1
+ *                  (a CTA pair), or 2 x 2 with multicast.
  *  stages          depth of the shared-memory ring.
- *  multicast       1 if operand panels are TMA-multicast inside a cluster.
+ *  multicast       0 (the planner's choice) or 1: split TF32 and TF32 with CTA
+ *                  pairs only (tile 256 x 256, cluster 2 x 2, deepest ring, A
+ *                  split by the pre-pass).  A cluster then holds two CTA pairs
+ *                  that compute horizontally adjacent tiles; each pair
+ *                  TMA-loads half of the A rows both need and multicasts it
+ *                  to both pairs, so A crosses from L2 once per two tiles.
+ *                  Results equal the pair kernel's bit for bit on tiles
+ *                  computed whole.  Measured slower than the pair kernel on
+ *                  GB300 (7 to 23 %), so the planner leaves it off.
  *  super_m/_n      super-tile: the output tiles are walked super-tile by
  *                  super-tile (an L2-locality group on one GPU).
  *  super_k         K chunk of the cluster split: super_k < K runs an init

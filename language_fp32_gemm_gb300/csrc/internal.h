@@ -99,6 +99,11 @@ struct TcArgs {
   // and the kernel splits it into tf32 big/small in shared memory; tmap_as is
   // unused.  0: both A maps point at the pre-split workspace.
   int a_inline;
+  // CTA-pair kernels only.  1: clusters of two pairs computing tiles (tm, 2 tn)
+  // and (tm, 2 tn + 1), which TMA-multicast their shared A panels: tiles_n
+  // counts such tile pairs, the A maps have 64-row boxes, grid_units counts
+  // clusters, and partials slots are per pair (slot 2 w + pair of worker w).
+  int multicast;
   float *partials;
   unsigned *flags;
   unsigned epoch;
@@ -118,6 +123,9 @@ int tc_max_stages(int passes, int bn);
 cudaError_t launch_tc_pair(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
                            int kind = kTcTf32);
 int tc_pair_max_stages(int passes, int bn);
+// Clusters of the multicast pair kernel (passes 1 or 3, bn 256, deepest ring)
+// that can be resident at once on the current device; -1 if the query failed.
+int tc_multicast_clusters(int passes, int bn, cudaStream_t stream);
 
 // Frees the workspace cached for `stream` on the current device (stream-ordered);
 // for code in this library that destroys a stream it created.

@@ -139,6 +139,9 @@ struct DeviceState {
   bool supported = false;
   int sm_count = 0;
   int *err = nullptr;  // device status word
+  // resident clusters of the multicast pair kernel, one pass / three passes
+  // (0 = not queried yet)
+  int mc_clusters[2] = {0, 0};
 };
 std::map<int, DeviceState> g_devices;
 
@@ -364,7 +367,14 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (math == PHOBOS_MATH_FP16 && p.path != PHOBOS_PATH_FP16) return PHOBOS_ERR_INVALID_VALUE;
   if (math == PHOBOS_MATH_BF16 && p.path != PHOBOS_PATH_BF16) return PHOBOS_ERR_INVALID_VALUE;
   if (math == PHOBOS_MATH_DEFAULT && half_path(p.path)) return PHOBOS_ERR_INVALID_VALUE;
-  if (p.cluster_n != 1 || p.multicast != 0 || (p.cluster_m != 1 && p.cluster_m != 2))
+  if (p.multicast != 0 && p.multicast != 1) return PHOBOS_ERR_INVALID_VALUE;
+  const bool mc = p.multicast == 1;
+  // multicast: two CTA pairs side by side along N (cluster 2 x 2), tf32 operands
+  // split by the pre-pass
+  if ((p.cluster_m != 1 && p.cluster_m != 2) || p.cluster_n != (mc ? 2 : 1))
+    return PHOBOS_ERR_UNSUPPORTED;
+  if (mc && (p.cluster_m != 2 || (p.path != PHOBOS_PATH_TF32 && p.path != PHOBOS_PATH_3XTF32) ||
+             p.a_split == 2))
     return PHOBOS_ERR_UNSUPPORTED;
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
   if (p.tail_split < 0 || p.tail_split > kMaxTailSplit) return PHOBOS_ERR_INVALID_VALUE;
@@ -383,7 +393,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
       return PHOBOS_ERR_INVALID_VALUE;
     const int max_st = pair ? tc_pair_max_stages(passes, p.tile_n) : tc_max_stages(passes, p.tile_n);
     if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
-    if (p.a_split == 2 && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
+    if ((p.a_split == 2 || mc) && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
     // 16-bit inputs: pre-converted A, deepest ring
     if (half_path(p.path) && (p.a_split == 2 || (p.stages != max_st && p.stages != 4)))
       return PHOBOS_ERR_INVALID_VALUE;
@@ -467,6 +477,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
                        int device, bool reuse_b = false) {
   const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
   const bool pair = p.cluster_m == 2;
+  const bool mc = p.multicast == 1;  // clusters of two pairs sharing A (validated: pairs, tf32)
   const int bm = pair ? 2 * kTcBM : kTcBM;
   const int bn = p.tile_n;
   const bool half = half_path(p.path);
@@ -482,7 +493,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   } else if (p.a_split == 2) {
     if (!a_tma_ok) return PHOBOS_ERR_UNSUPPORTED;
     a_inline = true;
-  } else if (p.a_split == 0) {
+  } else if (p.a_split == 0 && !mc) {
     const int max_st = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
     a_inline = a_tma_ok && N <= kInlineSplitMaxN && p.stages == max_st;
   }
@@ -491,16 +502,29 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   // workspace: [B big][B small][A big][A small] (no A part when A is split in-kernel)
   const size_t ops_bytes = static_cast<size_t>(ops * b_bytes + (a_inline ? 0 : ops * a_bytes));
 
-  // Persistent grid: one CTA (pair) per SM (pair).  The tiles of the last,
-  // partial wave are split along K so that idle SMs share the tail.
-  const int units = pair ? dev.sm_count / 2 : dev.sm_count;
-  const int total_tiles = static_cast<int>((Mp / bm) * (Np / bn));
+  // Persistent grid: one CTA (pair) per SM (pair), or one multicast cluster
+  // per four SMs, as many as can be resident together.  The tiles of the
+  // last, partial wave are split along K so that idle SMs share the tail.
+  // With multicast a tile of the walk is two pair tiles side by side.
+  int units = pair ? dev.sm_count / 2 : dev.sm_count;
+  if (mc) {
+    int &resident = dev.mc_clusters[passes == 3 ? 1 : 0];
+    if (resident == 0) resident = tc_multicast_clusters(passes, bn, stream);
+    if (resident <= 0) return PHOBOS_ERR_CUDA;
+    units = dev.sm_count / 4 < resident ? dev.sm_count / 4 : resident;
+    if (units <= 0) return PHOBOS_ERR_UNSUPPORTED;
+    if (env_flag("PHOBOS_LOG"))
+      std::fprintf(stderr, "[phobos] multicast clusters: %d resident at once, %d used\n", resident,
+                   units);
+  }
+  const int64_t walk_n = mc ? (Np / bn + 1) / 2 : Np / bn;  // tile columns of the walk
+  const int total_tiles = static_cast<int>((Mp / bm) * walk_n);
   const int chunk_blocks_max =
       static_cast<int>(round_up(p.super_k < K ? p.super_k : K, bk) / bk);
   const int tail = units > 0 ? total_tiles % units : 0;
   const int tail_units = tail_workers(p.tail_split, tail, units, chunk_blocks_max);
   const int full_tiles = tail_units > 0 ? total_tiles - tail : total_tiles;
-  const int64_t slots = tail_units;  // one partial sum per worker at most
+  const int64_t slots = static_cast<int64_t>(tail_units) * (mc ? 2 : 1);  // one partial sum per pair at most
   const size_t part_bytes = static_cast<size_t>(round_up(slots * bm * bn * 4, 256));
   const size_t flag_bytes = static_cast<size_t>(round_up(slots * 2 * kEpiWarps * 4, 256));
   const size_t need = ops_bytes + part_bytes + flag_bytes;
@@ -561,14 +585,17 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   TcArgs t{};
   // each CTA loads 128 rows of A and, in a pair, half of the tile's B rows
   const int b_box = pair ? bn / 2 : bn;
+  // with multicast each CTA loads half of its 128 A rows (and receives the
+  // other half from the other pair)
+  const int a_box = mc ? kTcBM / 2 : kTcBM;
   if (a_inline) {
     // the caller's A: K x M extents with its own stride; TMA fills zeros outside
     if ((st = make_kmajor_map_strided(&t.tmap_ab, A, M, K, lda, kTcBM)) != PHOBOS_OK) return st;
     t.tmap_as = t.tmap_ab;
   } else {
-    if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, kTcBM, kind)) != PHOBOS_OK) return st;
+    if ((st = make_kmajor_map(&t.tmap_ab, a_big, Mp, Kp, a_box, kind)) != PHOBOS_OK) return st;
     t.tmap_as = t.tmap_ab;
-    if (passes == 3 && (st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, kTcBM)) != PHOBOS_OK)
+    if (passes == 3 && (st = make_kmajor_map(&t.tmap_as, a_small, Mp, Kp, a_box)) != PHOBOS_OK)
       return st;
   }
   if ((st = make_kmajor_map(&t.tmap_bb, b_big, Np, Kp, b_box, kind)) != PHOBOS_OK) return st;
@@ -576,12 +603,13 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   if (passes == 3 && (st = make_kmajor_map(&t.tmap_bs, b_small, Np, Kp, b_box)) != PHOBOS_OK)
     return st;
   t.a_inline = a_inline ? 1 : 0;
+  t.multicast = mc ? 1 : 0;
   t.C = C;
   t.ldc = ldc;
   t.M = static_cast<int>(M);
   t.N = static_cast<int>(N);
   t.tiles_m = static_cast<int>(Mp / bm);
-  t.tiles_n = static_cast<int>(Np / bn);
+  t.tiles_n = static_cast<int>(walk_n);
   int64_t gm = p.super_m / bm;
   if (gm < 1) gm = 1;
   if (gm > t.tiles_m) gm = t.tiles_m;

@@ -183,11 +183,13 @@ struct RawAPrefetch {
   }
 };
 
-template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32>
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32,
+          bool MC = false>
 __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(KIND == kTcTf32 || (PASSES == 1 && !ASPLIT), "16-bit inputs: one pass, pre-converted");
+  static_assert(!MC || (PAIR && !ASPLIT && KIND == kTcTf32), "multicast: pre-split tf32 pairs");
   static_assert((4 * STAGES + 5) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   // K elements per 128-byte stage row: 32 fp32/tf32 or 64 fp16/bf16.
   constexpr int kBKE = KIND == kTcTf32 ? kBK : 2 * kBK;
@@ -213,25 +215,51 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  // Cluster layout: one CTA, one CTA pair (ranks 0, 1), or with multicast two
+  // pairs (ranks 0, 1 and 2, 3) that compute horizontally adjacent tiles and
+  // share their A panels.
+  constexpr uint32_t kCtas = MC ? 4u : PAIR ? 2u : 1u;
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t rank = MC ? (crank & 1u) : crank;  // rank inside the CTA pair
+  const uint32_t pp = MC ? (crank >> 1) : 0u;       // which pair of a multicast cluster
+  const uint32_t lead = MC ? (crank & ~1u) : 0u;    // cluster rank of this pair's leader
   const bool leader = rank == 0;
 
-  // Raise the abort flag of the peer CTA too, so both stop promptly.
+  // Raise the abort flag of the other CTAs of the cluster too, so all stop promptly.
   auto abort_peer = [&]() {
-    if (PAIR) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u), 1u);
+    const uint32_t flag = smem_u32(const_cast<int *>(abort_flag));
+    if (MC) {
+      for (uint32_t r = 0; r < kCtas; ++r)
+        if (r != crank) st_shared_cluster_u32(mapa_shared(flag, r), 1u);
+    } else if (PAIR) {
+      st_shared_cluster_u32(mapa_shared(flag, rank ^ 1u), 1u);
+    }
   };
 
-  // Persistent: each CTA (pair) walks the output tiles unit, unit + units, ...
-  // in raster order, so the tiles in flight at one time are neighbours.
+  // Persistent: each CTA (pair, or pair of pairs) walks the output tiles
+  // unit, unit + units, ... in raster order, so the tiles in flight at one
+  // time are neighbours.  With multicast a tile of the walk is two pair tiles
+  // side by side (tile columns 2 tn and 2 tn + 1); pair pp computes the second.
   constexpr int kTileM = PAIR ? 2 * kBM : kBM;
-  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int unit = static_cast<int>(blockIdx.x / kCtas);
+  const int units = static_cast<int>(gridDim.x / kCtas);
+  auto tile_coords = [&](int t, int &tm, int &tn) {
+    raster(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    if (MC) tn = 2 * tn + static_cast<int>(pp);
+  };
+  // Tail split: the partial-sum slot of worker w (one per pair of a
+  // multicast cluster).
+  auto slot_of = [&](int w) -> long long {
+    return MC ? 2ll * w + static_cast<long long>(pp) : static_cast<long long>(w);
+  };
   const int chunk = p.promote_blocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, 1);
+      // multicast: the leader's full barrier also takes the peer's relay, and
+      // every empty barrier takes both pairs' MMA commits
+      mbar_init(full0 + 8u * s, MC && leader ? 2 : 1);
+      mbar_init(empty0 + 8u * s, MC ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full0 + 8u * b, 1);
@@ -339,7 +367,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       for (int j = 0; j < kRawAPrefetchAhead; ++j) pf.step(p, unit, units, rank);
       for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
         int tm, tn;
-        raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        tile_coords(u.tile, tm, tn);
         const int m0 = tm * kTileM + static_cast<int>(rank) * kBM;
         const int b_row = tn * BN + static_cast<int>(rank) * S::kBRows;
         for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
@@ -360,7 +388,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
           tma_load_2d(st, &p.tmap_ab, af, kc, m0);  // raw A, zero outside the matrix
           if (PAIR) {
             if (leader) mbar_arrive_expect_tx(full, 2 * S::kOps * S::kBTile);
-            const uint32_t lead_full = mapa_shared(full, 0);
+            const uint32_t lead_full = mapa_shared(full, lead);
             tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
             if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
           } else {
@@ -399,7 +427,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       Unit u;
       for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
         int tm, tn;
-        raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        tile_coords(u.tile, tm, tn);
         const int m0 = tm * kTileM + static_cast<int>(rank) * kBM;
         const int b_row = tn * BN + static_cast<int>(rank) * S::kBRows;
         for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
@@ -417,10 +445,26 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
           const int kc = (p.k_block0 + kb) * kBKE;
           const uint32_t st = tiles + s * S::kStageBytes;
           const uint32_t bt = st + S::kOps * S::kATile;
-          if (PAIR) {
+          if (MC) {
+            // This CTA's 128 rows of A are the same in both pairs: each pair
+            // loads half of them (64 rows) and multicasts it to the CTA of
+            // the same rank in both pairs; every CTA's A bytes complete on its
+            // own full barrier (the peer relays its completion to the leader).
+            // B stays per pair: both halves complete on the leader's barrier.
+            mbar_arrive_expect_tx(full, S::kOps * S::kATile + (leader ? 2 * S::kOps * S::kBTile : 0));
+            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+            const uint32_t a_dst = st + pp * (S::kATile / 2);
+            const int a_row = m0 + static_cast<int>(pp) * (kBM / 2);
+            tma_load_2d_multicast(a_dst, &p.tmap_ab, full, kc, a_row, mask);
+            if (PASSES == 3)
+              tma_load_2d_multicast(a_dst + S::kATile, &p.tmap_as, full, kc, a_row, mask);
+            const uint32_t lead_full = mapa_shared(full, lead);
+            tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
+            if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
+          } else if (PAIR) {
             // both CTAs' bytes complete on the leader's barrier
             if (leader) mbar_arrive_expect_tx(full, 2 * S::kStageBytes);
-            const uint32_t lead_full = mapa_shared(full, 0);
+            const uint32_t lead_full = mapa_shared(full, lead);
             tma_load_2d_pair(st, &p.tmap_ab, lead_full, kc, m0);
             if (PASSES == 3) tma_load_2d_pair(st + S::kATile, &p.tmap_as, lead_full, kc, m0);
             tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
@@ -439,7 +483,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       // No bulk copy may still be writing shared memory at exit.  The leader's
       // full barriers count every armed stage; a pair's peer cannot observe its
       // own copies, so after an abort it gives them a bounded grace period.
-      if (leader) {
+      // With multicast every CTA's full barriers count its own A bytes.
+      if (leader || MC) {
         for (int s = 0; s < STAGES; ++s)
           if (armed & (1u << s))
             bounded_wait(full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
@@ -484,7 +529,10 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
           for (int first = 1; kb < kb_end; ++kb, ++g, first = 0) {
             const int s = g % STAGES;
             const uint32_t ph = (g / STAGES) & 1u;
-            if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma) ||
+            // with multicast the peer's relay (a cluster-scope release) also
+            // completes this barrier
+            if (!(MC ? bounded_wait_cluster(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)
+                     : bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) ||
                 (ASPLIT && !(PAIR ? bounded_wait_cluster(conv0 + 8u * s, ph, abort_flag, p.err,
                                                          kDevTimeoutMma)
                                   : bounded_wait(conv0 + 8u * s, ph, abort_flag, p.err,
@@ -529,14 +577,16 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
                   mma_f16(d_tmem, dab, dbb, idesc, acc);
               }
             }
+            // the slot is free once this pair's MMAs have read it; with
+            // multicast both pairs' CTAs wait for both pairs' commits
             if (PAIR)
-              mma_commit_pair(empty0 + 8u * s, 0x3);
+              mma_commit_pair(empty0 + 8u * s, MC ? 0xF : 0x3);
             else
               mma_commit(empty0 + 8u * s);
           }
           if (ok) {
             if (PAIR)
-              mma_commit_pair(acc_full0 + 8u * b, 0x3);
+              mma_commit_pair(acc_full0 + 8u * b, static_cast<uint16_t>(0x3u << lead));
             else
               mma_commit(acc_full0 + 8u * b);
           }
@@ -544,7 +594,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       }
       // Every MMA must be finished before TMEM is released.
       if (PAIR)
-        mma_commit_pair(mma_drained, 0x1);
+        mma_commit_pair(mma_drained, static_cast<uint16_t>(1u << lead));
       else
         mma_commit(mma_drained);
       bounded_wait(mma_drained, 0, abort_flag, p.err, kDevTimeoutDrain, false);
@@ -567,7 +617,28 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             ok = false;
             break;
           }
-          mbar_arrive_cluster(mapa_shared(conv0 + 8u * s, 0));
+          mbar_arrive_cluster(mapa_shared(conv0 + 8u * s, lead));
+        }
+      }
+    } else if (MC && lane == 0) {
+      // Relay, in the peer, with multicast: once this CTA's A half has landed
+      // (its own full barrier), arrive on the leader's full barrier, whose
+      // MMAs read that half.  The release at cluster scope orders the landing
+      // before the leader's acquire.
+      int g = 0;
+      bool ok = true;
+      Unit u;
+      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+        for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1u;
+          if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+          if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutProducer)) {
+            abort_peer();
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(mapa_shared(full0 + 8u * s, lead));
         }
       }
     }
@@ -583,7 +654,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
     float *sbuf = epi_stage + (warp - 2) * 32 * 32;  // this warp's 32 x 32 block of C
     for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
       int tm, tn;
-      raster(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      tile_coords(u.tile, tm, tn);
       // This warp owns rows row0 .. row0+31 and columns col0 .. col0+kHalf-1 of
       // the tile; lane l sums row row0 + l.
       const int tile_row = static_cast<int>(rank) * kBM + q * 32 + lane;  // 0 .. kTileM-1
@@ -648,7 +719,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         __syncwarp();
         if (lane == 0) {
           if (PAIR)
-            mbar_arrive_cluster(mapa_shared(acc_empty0 + 8u * b, 0));
+            mbar_arrive_cluster(mapa_shared(acc_empty0 + 8u * b, lead));
           else
             mbar_arrive(acc_empty0 + 8u * b);
         }
@@ -664,7 +735,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         // Hand the partial sum to the piece-0 owner through this worker's
         // slot, then release the flag once every accumulator thread's stores
         // are visible.
-        const long long slot = unit;
+        const long long slot = slot_of(unit);
         float4 *dst = reinterpret_cast<float4 *>(p.partials) +
                       ((slot * kRanks + rank) * kEpiWarps + (warp - 2)) * (kHalf / 4) * 32 + lane;
 #pragma unroll
@@ -686,7 +757,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         int w_end = unit + 1;
         while (w_end < p.tail_units && p.tail_tile[w_end] == tt) ++w_end;
         for (int w2 = unit + 1; w2 < w_end && ok; ++w2) {
-          const unsigned *flag = p.flags + (static_cast<long long>(w2) * 2 + rank) * kEpiWarps + (warp - 2);
+          const unsigned *flag = p.flags + (slot_of(w2) * 2 + rank) * kEpiWarps + (warp - 2);
           if (ld_acquire_gpu(flag) != p.epoch) {
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t polls = 1; ld_acquire_gpu(flag) != p.epoch; ++polls) {
@@ -721,10 +792,12 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         static_assert(kBufs >= 2 && kSlotF4 % kChunkF4 == 0, "fix-up staging fits the ring");
         const uint32_t stage = tiles + ((warp - 2) * (kBufs * kChunkF4 * 32) + lane) * 16u;
         const float4 *part0 = reinterpret_cast<const float4 *>(p.partials) +
-                              ((static_cast<long long>(unit + 1) * kRanks + rank) * kEpiWarps + (warp - 2)) *
+                              ((slot_of(unit + 1) * kRanks + rank) * kEpiWarps + (warp - 2)) *
                                   (kSlotF4 * 32) + lane;
-        // the pieces' slots are consecutive: piece i of this warp at part0 + i * kSlotStride
-        constexpr long long kSlotStride = static_cast<long long>(kRanks) * kEpiWarps * kSlotF4 * 32;
+        // the pieces' slots are consecutive (every other slot with multicast):
+        // piece i of this warp at part0 + i * kSlotStride
+        constexpr long long kSlotStride =
+            static_cast<long long>(MC ? 2 : 1) * kRanks * kEpiWarps * kSlotF4 * 32;
         const int n_chunks = (w_end - unit - 1) * kCps;
         auto issue = [&](int c) {
           if (c < n_chunks) {
@@ -839,17 +912,38 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
   }
 }
 
-template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32>
+// Launch configuration of one kernel instance: the persistent grid of `units`
+// CTAs, CTA pairs, or (multicast) clusters of two pairs.
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND, bool MC>
+void tc_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, unsigned units,
+               cudaStream_t stream) {
+  using S = TcShape<BN, PASSES, PAIR>;
+  const unsigned ctas = MC ? 4u : PAIR ? 2u : 1u;
+  cfg = {};
+  cfg.gridDim = dim3(ctas * units, 1, 1);
+  cfg.blockDim = dim3(threads_for(ASPLIT), 1, 1);
+  cfg.dynamicSmemBytes = S::smem_bytes(STAGES);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32,
+          bool MC = false>
 cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
-  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND>;
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC>;
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>(a.tiles_m) * a.tiles_n;
   // one CTA (pair) per SM (pair), never more than there are tiles
-  const long long workers = PAIR ? a.sm_count / 2 : a.sm_count;
+  const long long workers = MC ? a.sm_count / 4 : PAIR ? a.sm_count / 2 : a.sm_count;
   const unsigned units = a.grid_units > 0
                              ? static_cast<unsigned>(a.grid_units)
                              : static_cast<unsigned>(tiles < workers ? tiles : workers);
@@ -858,19 +952,27 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
     kern<<<units, threads_for(ASPLIT), smem, stream>>>(a);
     return cudaGetLastError();
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * units, 1, 1);
-  cfg.blockDim = dim3(threads_for(ASPLIT), 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
+  cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  tc_config<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC>(cfg, attr, units, stream);
   return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Multicast clusters (two CTA pairs, four SMs) that fit on the device at once.
+// The tail split makes a worker wait for others, so the persistent grid may not
+// hold more clusters than can be resident together.
+template <int BN, int PASSES, int STAGES>
+int mc_resident_clusters(cudaStream_t stream) {
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, true, false, kTcTf32, true>;
+  const int smem = TcShape<BN, PASSES, true>::smem_bytes(STAGES);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  tc_config<BN, PASSES, STAGES, true, false, kTcTf32, true>(cfg, attr, 1, stream);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return -1;
+  return n;
 }
 
 template <int BN, int PASSES, bool PAIR>
@@ -890,6 +992,14 @@ cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream, int 
     if (stages == 4 && kMax >= 4)
       return kind == kTcF16 ? launch_one<BN, 1, (kMax >= 4 ? 4 : 2), PAIR, false, kTcF16>(a, stream)
                             : launch_one<BN, 1, (kMax >= 4 ? 4 : 2), PAIR, false, kTcBf16>(a, stream);
+    return cudaErrorInvalidValue;
+  }
+  // Multicast clusters: pre-split operands, the deepest ring.
+  if (a.multicast) {
+    if constexpr (PAIR) {
+      if (a.a_inline || stages != kTop) return cudaErrorInvalidValue;
+      return launch_one<BN, PASSES, kTop, true, false, kTcTf32, true>(a, stream);
+    }
     return cudaErrorInvalidValue;
   }
   // In-kernel A split: always the deepest ring.
@@ -916,6 +1026,15 @@ int max_stages_of(int passes, int bn) {
 
 int tc_max_stages(int passes, int bn) { return max_stages_of<false>(passes, bn); }
 int tc_pair_max_stages(int passes, int bn) { return max_stages_of<true>(passes, bn); }
+
+int tc_multicast_clusters(int passes, int bn, cudaStream_t stream) {
+  if (bn != 256) return -1;
+  constexpr int k3 = TcShape<256, 3, true>::max_stages() > 6 ? 6 : TcShape<256, 3, true>::max_stages();
+  constexpr int k1 = TcShape<256, 1, true>::max_stages() > 6 ? 6 : TcShape<256, 1, true>::max_stages();
+  if (passes == 3) return mc_resident_clusters<256, 3, k3>(stream);
+  if (passes == 1) return mc_resident_clusters<256, 1, k1>(stream);
+  return -1;
+}
 
 cudaError_t launch_tc(const TcArgs &a, int passes, int bn, int stages, cudaStream_t stream,
                       int kind) {

@@ -109,3 +109,42 @@ def test_plan_paths(lib):
 def test_plan_rejects_unknown_math(lib):
     with pytest.raises(phobos.PhobosError):
         phobos.phobos_gemm_plan(16, 16, 16, 16, 16, 16, 9)
+
+
+def test_dimensions_beyond_the_kernels_int_range_are_refused(lib):
+    big = 1 << 31  # the kernels index rows and columns with 32-bit ints
+    with pytest.raises(phobos.PhobosError) as e:
+        phobos.phobos_gemm_plan(big, 4, 4, 4, 4, 4)
+    assert e.value.status == phobos.PHOBOS_ERR_UNSUPPORTED
+    assert phobos.phobos_sgemm(4, big, 4, 1.0, 16, big, 16, big, 0.0, 16, big, 0) == \
+        phobos.PHOBOS_ERR_UNSUPPORTED
+
+
+def test_multicast_plans_are_validated_before_any_device_call(lib):
+    M = N = K = 1024
+
+    def run(plan, math=phobos.PHOBOS_MATH_3XTF32):
+        return phobos.phobos_sgemm_ex(M, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0, math, plan)
+
+    def mc(math="3xtf32", **fields):
+        p = phobos.phobos_gemm_plan(M, N, K, K, N, N, math)
+        p.multicast, p.cluster_n = 1, 2
+        for name, value in fields.items():
+            setattr(p, name, value)
+        return p
+
+    assert run(mc(cluster_n=1)) == phobos.PHOBOS_ERR_UNSUPPORTED   # multicast needs 2 x 2
+    assert run(mc(multicast=2)) == phobos.PHOBOS_ERR_INVALID_VALUE
+    assert run(mc(a_split=2)) == phobos.PHOBOS_ERR_UNSUPPORTED     # A split inside the kernel
+    p = mc()
+    p.stages -= 1
+    assert run(p) == phobos.PHOBOS_ERR_INVALID_VALUE               # the deepest ring only
+    assert run(mc("bf16"), phobos.PHOBOS_MATH_BF16) == phobos.PHOBOS_ERR_UNSUPPORTED
+    p = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
+    p.cluster_n = 2                                                 # 2 x 2 without multicast
+    assert run(p) == phobos.PHOBOS_ERR_UNSUPPORTED
+    single = phobos.phobos_gemm_plan(128, N, K, K, N, N, "3xtf32")
+    assert single.cluster_m == 1
+    single.multicast, single.cluster_n = 1, 2                      # single CTAs: no pairs
+    assert phobos.phobos_sgemm_ex(128, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0,
+                                  phobos.PHOBOS_MATH_3XTF32, single) == phobos.PHOBOS_ERR_UNSUPPORTED

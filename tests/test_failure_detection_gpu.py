@@ -2,11 +2,12 @@
 
 Every mbarrier wait in the tensor-core kernel is bounded (about two seconds);
 when one expires the kernel records where in a device status word, stops all
-of its roles (both CTAs of a pair), releases its tensor memory and returns.
-PHOBOS_TEST_WITHHOLD_LOAD=1 makes the producer skip the first operand load, so
-the MMA issuer's wait for it runs out.  The test checks that the host reads
-PHOBOS_ERR_TIMEOUT and that the context stays usable: the next call is
-correct.  Nothing here faults, traps or hangs the GPU.
+of its roles (in every CTA of a pair or multicast cluster), releases its
+tensor memory and returns.  PHOBOS_TEST_WITHHOLD_LOAD=1 makes the producer
+skip the first operand load, so the MMA issuer's wait for it runs out.  The
+test checks that the host reads PHOBOS_ERR_TIMEOUT and that the context stays
+usable: the next call is correct.  Nothing here faults, traps or hangs the
+GPU.
 """
 import numpy as np
 import pytest
@@ -30,25 +31,29 @@ def dev():
     return d
 
 
-@pytest.mark.parametrize("shape", [(128, 256, 96), (256, 256, 96)], ids=["single_cta", "cta_pair"])
-def test_expired_wait_is_reported_and_context_survives(dev, shape, monkeypatch):
+@pytest.mark.parametrize("shape,multicast", [((128, 256, 96), 0), ((256, 256, 96), 0),
+                                             ((256, 512, 96), 1)],
+                         ids=["single_cta", "cta_pair", "multicast_cluster"])
+def test_expired_wait_is_reported_and_context_survives(dev, shape, multicast, monkeypatch):
     M, N, K = shape
     plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
     assert plan.cluster_m == (2 if M > 128 else 1)
+    if multicast:  # two CTA pairs sharing A through TMA multicast
+        plan.multicast, plan.cluster_n = 1, 2
     A = si.normal(71, 0, (M, K))
     B = si.normal(71, 1, (K, N))
     dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
     dC = torch.full((M, N), 5.0, device=dev)
     assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK  # nothing pending
     monkeypatch.setenv("PHOBOS_TEST_WITHHOLD_LOAD", "1")
-    phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32")
+    phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32", plan=plan)
     st = phobos.phobos_check_device(0)
     monkeypatch.delenv("PHOBOS_TEST_WITHHOLD_LOAD")
     assert st == phobos.PHOBOS_ERR_TIMEOUT, phobos.status_string(st)
     assert bool((dC == 5.0).all())  # the aborted kernel wrote nothing
     assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK  # the word was cleared
     # the context is intact: a normal call gives the right answer
-    phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32")
+    phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32", plan=plan)
     assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK
     ref, den = oracle.sgemm(A, B, None, 1.0, 0.0)
     assert oracle.max_rel_error(dC.cpu().numpy(), ref, den) <= oracle.TOL_FP32
