@@ -106,8 +106,11 @@ typedef enum {
  *                  TMA-loads half of the A rows both need and multicasts it
  *                  to both pairs, so A crosses from L2 once per two tiles.
  *                  Results equal the pair kernel's bit for bit on tiles
- *                  computed whole.  Measured slower than the pair kernel on
- *                  GB300 (7 to 23 %), so the planner leaves it off.
+ *                  computed whole.  Only as many clusters as fit on the GPU
+ *                  at once are launched (36 on GB300, i.e. 144 of the 152
+ *                  SMs), so the planner leaves it off: measured against the
+ *                  pair kernel it is 5 % slower at 8192^3, 10 % at 4096^3 and
+ *                  even at 16384^3.
  *  super_m/_n      super-tile: the output tiles are walked super-tile by
  *                  super-tile (an L2-locality group on one GPU).
  *  super_k         K chunk of the cluster split: super_k < K runs an init

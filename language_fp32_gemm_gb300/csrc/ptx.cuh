@@ -105,19 +105,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
       : "memory");
 }
 
-// The same box, written to offset `dst` of every CTA of the cluster named in
-// `cta_mask` (bit r = cluster rank r); each of them gets the completion on its
-// own mbarrier at offset `bar`.  dst and bar are this CTA's shared addresses.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void *tmap,
-                                                      uint32_t bar, int32_t c0, int32_t c1,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
-
 // Bring one box of a tensor map into L2 (no shared memory, no barrier); the
 // x coordinate follows the same 16-byte rule as a load.
 __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, int32_t c1) {
@@ -339,6 +326,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Multicast form of tma_load_2d_pair: the box lands at offset `dst` of every
+// CTA in `cta_mask`, and each destination's bytes complete on the mbarrier at
+// the offset of `bar_cluster` in the leader CTA of the destination's pair
+// (bar_cluster names the barrier in a leader, even cluster rank).
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const void *tmap,
+                                                           uint32_t bar_cluster, int32_t c0,
+                                                           int32_t c1, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask)
       : "memory");
 }
 

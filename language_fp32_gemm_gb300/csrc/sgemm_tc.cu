@@ -256,9 +256,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // multicast: the leader's full barrier also takes the peer's relay, and
-      // every empty barrier takes both pairs' MMA commits
-      mbar_init(full0 + 8u * s, MC && leader ? 2 : 1);
+      // multicast: every empty barrier takes both pairs' MMA commits
+      mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, MC ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -448,17 +447,17 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
           if (MC) {
             // This CTA's 128 rows of A are the same in both pairs: each pair
             // loads half of them (64 rows) and multicasts it to the CTA of
-            // the same rank in both pairs; every CTA's A bytes complete on its
-            // own full barrier (the peer relays its completion to the leader).
-            // B stays per pair: both halves complete on the leader's barrier.
-            mbar_arrive_expect_tx(full, S::kOps * S::kATile + (leader ? 2 * S::kOps * S::kBTile : 0));
+            // the same rank in both pairs.  Every byte that lands in a pair
+            // completes on its leader's full barrier, as in the pair kernel.
+            // B stays per pair.
+            if (leader) mbar_arrive_expect_tx(full, 2 * S::kStageBytes);
             const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
             const uint32_t a_dst = st + pp * (S::kATile / 2);
             const int a_row = m0 + static_cast<int>(pp) * (kBM / 2);
-            tma_load_2d_multicast(a_dst, &p.tmap_ab, full, kc, a_row, mask);
-            if (PASSES == 3)
-              tma_load_2d_multicast(a_dst + S::kATile, &p.tmap_as, full, kc, a_row, mask);
             const uint32_t lead_full = mapa_shared(full, lead);
+            tma_load_2d_pair_multicast(a_dst, &p.tmap_ab, lead_full, kc, a_row, mask);
+            if (PASSES == 3)
+              tma_load_2d_pair_multicast(a_dst + S::kATile, &p.tmap_as, lead_full, kc, a_row, mask);
             tma_load_2d_pair(bt, &p.tmap_bb, lead_full, kc, b_row);
             if (PASSES == 3) tma_load_2d_pair(bt + S::kBTile, &p.tmap_bs, lead_full, kc, b_row);
           } else if (PAIR) {
@@ -483,8 +482,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       // No bulk copy may still be writing shared memory at exit.  The leader's
       // full barriers count every armed stage; a pair's peer cannot observe its
       // own copies, so after an abort it gives them a bounded grace period.
-      // With multicast every CTA's full barriers count its own A bytes.
-      if (leader || MC) {
+      if (leader) {
         for (int s = 0; s < STAGES; ++s)
           if (armed & (1u << s))
             bounded_wait(full0 + 8u * s, (last_parity >> s) & 1u, abort_flag, p.err,
@@ -529,10 +527,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
           for (int first = 1; kb < kb_end; ++kb, ++g, first = 0) {
             const int s = g % STAGES;
             const uint32_t ph = (g / STAGES) & 1u;
-            // with multicast the peer's relay (a cluster-scope release) also
-            // completes this barrier
-            if (!(MC ? bounded_wait_cluster(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)
-                     : bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma)) ||
+            if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutMma) ||
                 (ASPLIT && !(PAIR ? bounded_wait_cluster(conv0 + 8u * s, ph, abort_flag, p.err,
                                                          kDevTimeoutMma)
                                   : bounded_wait(conv0 + 8u * s, ph, abort_flag, p.err,
@@ -618,27 +613,6 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
             break;
           }
           mbar_arrive_cluster(mapa_shared(conv0 + 8u * s, lead));
-        }
-      }
-    } else if (MC && lane == 0) {
-      // Relay, in the peer, with multicast: once this CTA's A half has landed
-      // (its own full barrier), arrive on the leader's full barrier, whose
-      // MMAs read that half.  The release at cluster scope orders the landing
-      // before the leader's acquire.
-      int g = 0;
-      bool ok = true;
-      Unit u;
-      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
-        for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
-          const int s = g % STAGES;
-          const uint32_t ph = (g / STAGES) & 1u;
-          if (p.withhold_first_load && g == 0) continue;  // failure-detection test
-          if (!bounded_wait(full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutProducer)) {
-            abort_peer();
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(mapa_shared(full0 + 8u * s, lead));
         }
       }
     }
