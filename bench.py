@@ -44,6 +44,9 @@ def parse_args():
     ap.add_argument("--workload", default="sgemm_8192")
     ap.add_argument("--math", default="default",
                     choices=["default", "3xtf32", "tf32", "ffma", "fp16", "bf16"])
+    ap.add_argument("--multicast", action="store_true",
+                    help="device-resident steps use the plan's multicast clusters (two CTA "
+                         "pairs sharing A); the e2e leg keeps the automatic plan")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target host time of the oracle baseline sample")
@@ -85,10 +88,11 @@ def peak_for(path_name, peaks):
             "152 SMs x 128 fp32 lanes x 2 flop x max SM clock")
 
 
-def kernel_traffic(kernel_file, workload, math_name):
+def kernel_traffic(kernel_file, workload, math_name, multicast=False):
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
     or None when the kernel source changed since the counters were taken."""
-    summary = os.path.join(ROOT, "profiles", "sgemm_tc_%s_%s.md" % (math_name, workload))
+    summary = os.path.join(ROOT, "profiles", "sgemm_tc_%s%s_%s.md"
+                           % (math_name, "_multicast" if multicast else "", workload))
     try:
         text = open(summary).read()
     except OSError:
@@ -283,13 +287,16 @@ def run_phobos(args):
     dC0 = C_p.to(dev)
     dC = dC0.clone()
     plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, args.math)
+    if args.multicast:
+        plan.multicast, plan.cluster_n = 1, 2
     path_name = {phobos.PHOBOS_PATH_FFMA: "ffma", phobos.PHOBOS_PATH_TF32: "tf32",
                  phobos.PHOBOS_PATH_3XTF32: "3xtf32", phobos.PHOBOS_PATH_FP16: "fp16",
                  phobos.PHOBOS_PATH_BF16: "bf16"}[plan.path]
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        phobos.sgemm(dA, dB, dC, w.alpha, w.beta, math=args.math, stream=stream)
+        phobos.sgemm(dA, dB, dC, w.alpha, w.beta, math=args.math, stream=stream,
+                     plan=plan if args.multicast else None)
 
     for _ in range(args.warmup):
         step()
@@ -386,7 +393,7 @@ def run_phobos(args):
         per_clock = {"3xtf32": tf32_clk / 3.0, "tf32": tf32_clk}.get(path_name, 2 * tf32_clk)
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": kernel_traffic(kernel_file, args.workload,
-                                                                    path_name),
+                                                                    path_name, args.multicast),
                 "peak_source": "%s (%s)" % (peak_src, peak_note),
                 "kernel": "sgemm_tc_kernel" if path_name != "ffma" else "sgemm_ffma_kernel",
                 "kernel_ms": avg_kernel_ms,
