@@ -91,8 +91,11 @@ def peak_for(path_name, peaks):
 def kernel_traffic(kernel_file, workload, math_name, multicast=False):
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
     or None when the kernel source changed since the counters were taken."""
-    summary = os.path.join(ROOT, "profiles", "sgemm_tc_%s%s_%s.md"
-                           % (math_name, "_multicast" if multicast else "", workload))
+    if math_name == "ffma":
+        summary = os.path.join(ROOT, "profiles", "sgemm_ffma_%s.md" % workload)
+    else:
+        summary = os.path.join(ROOT, "profiles", "sgemm_tc_%s%s_%s.md"
+                               % (math_name, "_multicast" if multicast else "", workload))
     try:
         text = open(summary).read()
     except OSError:

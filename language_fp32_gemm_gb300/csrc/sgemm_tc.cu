@@ -43,7 +43,15 @@
 //    each SM reads its B half once for both tensor cores, which halves the
 //    per-SM operand traffic of the single-CTA tile.  Commits are multicast to
 //    both CTAs; the peer's epilogue warps arrive on the leader's barriers
-//    through distributed shared memory.  No TMA multicast is used.
+//    through distributed shared memory.
+//  - Multicast clusters (MC = true, an opt-in plan): a cluster of four CTAs
+//    holds two pairs that compute horizontally adjacent tiles, i.e. one
+//    super-tile of 256 x 512 (the "@cluster" page's super-tile as a
+//    thread-block cluster; "Clusters et DSMEM", section 3.5, TMA multicast).
+//    Both pairs need the same A rows: each pair TMA-loads half of them and
+//    multicasts them into the rings of both pairs, so A crosses from L2 once
+//    per two tiles.  A ring slot is free once both pairs' MMAs have read it:
+//    each leader's commit arrives on the empty barriers of all four CTAs.
 //
 // The kernel is persistent: one CTA (or CTA pair) per SM (pair) loops over the
 // output tiles with a static stride.  Ring slots, phases and TMEM buffers run
