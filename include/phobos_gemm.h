@@ -127,7 +127,9 @@ typedef enum {
  *                  the persistent grid is cut along K into pieces for the
  *                  CTAs (pairs) that would otherwise idle (0 = automatic:
  *                  about sqrt(K / 80) pieces, as many as the idle CTAs
- *                  allow, at most 8; 1 = off; S = 2..8: S pieces per tile,
+ *                  allow, at most 8, or, for K <= 4096 when those whole
+ *                  pieces would leave a fifth of the CTAs idle, one more
+ *                  piece per tile; 1 = off; S = 2..8: S pieces per tile,
  *                  or, when fewer than S CTAs per tail tile are free, the
  *                  tail's K blocks dealt evenly to every CTA).  Every piece
  *                  spans at least K = 128.  Results are equal up to rounding

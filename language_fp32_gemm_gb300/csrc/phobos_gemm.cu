@@ -82,12 +82,23 @@ int tail_workers(int split, int tail, int units, int k_blocks) {
     // 0.8 us): k_blocks / S + 2.5 * (S - 1) is least at S = sqrt(k_blocks / 2.5).
     S = static_cast<int>(std::lround(std::sqrt(k_blocks / 2.5)));
     if (S > kMaxTailSplit) S = kMaxTailSplit;
-    // Whole pieces only: every tail tile is then cut at the same K offsets, so
+    // Whole pieces: every tail tile is then cut at the same K offsets, so
     // tiles that share an A or B panel read it at the same time, as whole
     // tiles do.  Even shares across tile boundaries put concurrent pieces at
     // different K offsets: on a 1024 x 8192 x 8192 band the tail then read its
     // B panels from DRAM again and the kernel took 500 us instead of 438 us.
-    if (S > units / tail) S = units / tail;
+    // With short K that costs less than leaving SMs idle: when whole pieces
+    // would leave a fifth of the workers idle and K is at most 128 blocks,
+    // one more piece per tile deals the tail evenly to every worker.
+    // Measured on GB300 (main kernel, 28 tail tiles over 76 pairs, 128 K
+    // blocks): 4096^3 390 us instead of 404 (beta 0) and 405 instead of 416
+    // (beta 1), 65536 x 256 x 4096 441 instead of 472.  With 256 K blocks
+    // (8192^3, 36 tail tiles) the even shares were no faster.
+    const int whole = units / tail;
+    if (S > whole) {
+      const bool idle_fifth = static_cast<int64_t>(tail) * whole * 5 <= static_cast<int64_t>(units) * 4;
+      S = (k_blocks <= 128 && idle_fifth) ? whole + 1 : whole;
+    }
   }
   if (S > k_blocks / kMinPieceBlocks) S = k_blocks / kMinPieceBlocks;
   if (S < 2) return 0;
