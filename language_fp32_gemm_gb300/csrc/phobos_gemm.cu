@@ -743,8 +743,7 @@ extern "C" {
 phobos_status_t phobos_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                  int64_t ldc, phobos_math_t math, phobos_gemm_plan_t *out) {
   if (!out) return PHOBOS_ERR_INVALID_VALUE;
-  phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
-  if (st == PHOBOS_ERR_UNSUPPORTED) return st;
+  const phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
   if (st != PHOBOS_OK) return st;
   return make_plan(M, N, K, math, out);
 }

@@ -148,3 +148,17 @@ def test_multicast_plans_are_validated_before_any_device_call(lib):
     single.multicast, single.cluster_n = 1, 2                      # single CTAs: no pairs
     assert phobos.phobos_sgemm_ex(128, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0,
                                   phobos.PHOBOS_MATH_3XTF32, single) == phobos.PHOBOS_ERR_UNSUPPORTED
+
+
+def test_missing_library_raises_instead_of_falling_back():
+    # No CPU fallback: without the built library every entry point raises.
+    code = ("import language_fp32_gemm_gb300 as p\n"
+            "p.LIBRARY_PATH = '/nonexistent/libphobos_gemm.so'\n"
+            "try:\n"
+            "    p.phobos_sgemm(4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, 0)\n"
+            "except ImportError as e:\n"
+            "    print('raised:', e)\n")
+    out = subprocess.run(["python", "-c", code], cwd=ROOT, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert "raised: libphobos_gemm.so is not built" in out.stdout
