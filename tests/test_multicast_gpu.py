@@ -80,6 +80,10 @@ def test_multicast_matches_oracle_and_pair_kernel(dev, math, shape):
     ((2560, 2560, 2048), 8, None),   # 50 cluster tiles: tail shares across tiles
     ((2500, 2510, 1100), 8, 512),    # the same inside K chunks, ragged edges
     ((520, 390, 2100), 0, 512),      # split inside every K chunk of the cluster split
+    # 3 tile columns: the second pair of each last cluster is past N, yet it
+    # still computes (zeros) and hands over its tail pieces
+    ((1000, 700, 2048), 0, None),
+    ((1000, 700, 2048), 3, None),
 ], ids=lambda v: str(v))
 def test_multicast_tail_split_and_k_chunks(dev, math, shape, split, super_k):
     M, N, K = shape
