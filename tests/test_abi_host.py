@@ -162,3 +162,20 @@ def test_missing_library_raises_instead_of_falling_back():
                          timeout=120)
     assert out.returncode == 0, out.stderr
     assert "raised: libphobos_gemm.so is not built" in out.stdout
+
+
+def test_binding_checks_tensors_before_any_call():
+    torch = pytest.importorskip("torch")
+    a = torch.zeros(4, 4)
+    with pytest.raises(TypeError):  # host tensors: the library takes device memory only
+        phobos.sgemm(a, a, a.clone())
+    # leading dimensions of row-major views; anything else is refused
+    big = torch.zeros(6, 10)
+    assert phobos._ld(big[:, :7], "A") == 10
+    assert phobos._ld(torch.zeros(1, 5), "A") == 5
+    with pytest.raises(ValueError):
+        phobos._ld(big.t(), "A")                      # column-major view
+    with pytest.raises(ValueError):
+        phobos._ld(torch.zeros(3), "A")               # not 2-D
+    with pytest.raises(ValueError):
+        phobos._ld(torch.zeros(16).as_strided((4, 4), (2, 1)), "A")  # overlapping rows
