@@ -52,3 +52,24 @@ def test_single_rank_needs_no_collective():
     import bench
     max_ms, gflops = bench.aggregate_rate(50.0, 1.0e9, 4, 1)
     assert max_ms == 50.0 and gflops == pytest.approx(4 * 1.0e9 / 0.05 / 1e9)
+
+
+def test_reference_arm_prints_one_contract_line():
+    # The reference arm (the CPU oracle on a row sample) runs without a GPU:
+    # its JSON line carries the keys the benchmark contract asks for.
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                          "sgemm_256", "--steps", "2", "--warmup", "1",
+                          "--reference-budget", "3"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GFLOP/s" and d["value"] > 0
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "sgemm_256"
