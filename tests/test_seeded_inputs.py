@@ -62,3 +62,29 @@ def test_workload_table():
     assert (w.M, w.N, w.K) == (3001, 5003, 1999)
     r, c = si.workload("sgemm_16384").samples()
     assert r.min() >= 0 and r.max() < 16384 and c.max() == 16383 and len(r) >= 4096
+
+
+def test_every_workload_matches_its_stated_recipe():
+    # (M, N, K, alpha, beta, seed, A, B, C_old) as the five benchmark workloads state them
+    want = {
+        "sgemm_256": (256, 256, 256, 1.5, 0.5, 0, "uniform", "uniform", "uniform"),
+        "sgemm_256_int": (256, 256, 256, 1.5, 0.5, 0, "int", "int", "int"),
+        "sgemm_4096_beta0": (4096, 4096, 4096, 1.0, 0.0, 1, "normal", "normal", "uniform"),
+        "sgemm_4096_beta1": (4096, 4096, 4096, 1.0, 1.0, 1, "normal", "normal", "uniform"),
+        "sgemm_8192": (8192, 8192, 8192, 0.75, 0.25, 2, "uniform", "uniform", "normal"),
+        "sgemm_3001x5003x1999": (3001, 5003, 1999, 1.0, 0.5, 3, "normal", "normal", "uniform"),
+        "sgemm_65536x256x4096": (65536, 256, 4096, 1.0, 0.5, 3, "normal", "normal", "uniform"),
+        "sgemm_16384": (16384, 16384, 16384, 1.0, 0.0, 4, "uniform", "uniform", "zeros"),
+    }
+    assert set(si.WORKLOADS) == set(want)
+    for name, (M, N, K, alpha, beta, seed, a, b, c) in want.items():
+        w = si.workload(name)
+        assert (w.M, w.N, w.K, w.alpha, w.beta, w.seed) == (M, N, K, alpha, beta, seed), name
+        assert (w.a[0], w.b[0], w.c[0]) == (a, b, c), name
+    # N(0, 1/sqrt(K)): the standard deviation is 1/sqrt(K)
+    for name in ("sgemm_3001x5003x1999", "sgemm_65536x256x4096"):
+        w = si.workload(name)
+        assert w.a[1] == w.b[1] == 1.0 / np.sqrt(w.K)
+    # the two shapes that share seed 3 draw from different streams
+    assert set(si.workload("sgemm_3001x5003x1999").streams).isdisjoint(
+        si.workload("sgemm_65536x256x4096").streams)
