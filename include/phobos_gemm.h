@@ -164,7 +164,8 @@ typedef struct {
  * attribute page, "A minimal kernel" and "What runs today" (a dimension takes
  * its first value without tuning); "Show HN: Phobos", "Clustering".
  * Errors: PHOBOS_ERR_INVALID_VALUE for bad sizes/leading dimensions, an
- * unknown math mode or out == NULL.
+ * unknown math mode or out == NULL; PHOBOS_ERR_UNSUPPORTED when M, N or K
+ * exceeds 2^31 - 1024 (the kernels index rows and columns with 32-bit ints).
  */
 phobos_status_t phobos_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda,
                                  int64_t ldb, int64_t ldc, phobos_math_t math,
@@ -184,7 +185,9 @@ phobos_status_t phobos_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
 /*
  * As phobos_sgemm with an explicit math mode and, optionally, a plan (NULL =
  * automatic).  A caller-supplied plan is validated against the shape and the
- * mode; PHOBOS_ERR_INVALID_VALUE if it does not fit.  A plan with
+ * mode before anything is enqueued: PHOBOS_ERR_INVALID_VALUE if a field is out
+ * of range for it, PHOBOS_ERR_UNSUPPORTED for a cluster shape this build does
+ * not run (see cluster_m/_n and multicast above).  A plan with
  * super_k < K runs the cluster split of the "@cluster" page ("the init leaf
  * zeroes the output super-tile, or scales it by beta, and the step leaf adds
  * one chunk of K per launch"; "Show HN: Phobos", "Clustering": the beta term
