@@ -46,7 +46,8 @@ def parse_args():
                     choices=["default", "3xtf32", "tf32", "ffma", "fp16", "bf16"])
     ap.add_argument("--multicast", action="store_true",
                     help="device-resident steps use the plan's multicast clusters (two CTA "
-                         "pairs sharing A); the e2e leg keeps the automatic plan")
+                         "pairs sharing A); the e2e leg keeps the automatic plan.  One GPU "
+                         "only: refused under a multi-rank launch")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target host time of the oracle baseline sample")
@@ -109,12 +110,49 @@ def kernel_traffic(kernel_file, workload, math_name, multicast=False):
     return int(m_tr.group(1))
 
 
+def code_only(text):
+    """C/C++ source with comments removed and every run of whitespace outside
+    string and character literals collapsed to one space, so that editing a
+    comment or re-indenting leaves it unchanged."""
+    out, code = [], []
+    i, n = 0, len(text)
+
+    def flush():
+        if code:
+            out.append(" ".join("".join(code).split()))
+            code.clear()
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            code.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            code.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            flush()
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            code.append(c)
+            i += 1
+    flush()
+    return " ".join(x for x in out if x)
+
+
 def kernel_source_sha256(kernel_file):
-    """SHA-256 over the kernel's source and the two headers it is built from."""
+    """SHA-256 over the code (comments and layout stripped, see code_only) of
+    the kernel's source and the two headers it is built from."""
     h = hashlib.sha256()
     for name in (kernel_file, "ptx.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "language_fp32_gemm_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "language_fp32_gemm_gb300", "csrc", name)) as f:
+            h.update(code_only(f.read()).encode())
+            h.update(b"\0")
     return h.hexdigest()
 
 
@@ -356,7 +394,9 @@ def run_phobos(args):
     # ------------------------------------------------ end to end, host buffers
     C_out = torch.empty_like(C_p).pin_memory()
     e2e_ms = []
-    for i in range(args.e2e_steps + 1):
+    # --e2e-steps 0 skips this leg (profiling commands that capture only the
+    # device-resident steps); the line's e2e is then null.
+    for i in range(args.e2e_steps + 1 if args.e2e_steps > 0 else 0):
         C_out.copy_(C_p)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -372,7 +412,9 @@ def run_phobos(args):
             e2e_ms.append(e0.elapsed_time(e1))
     h2d = 4 * (M * K + K * N + (M * N if w.beta != 0 else 0))
     d2h = 4 * M * N
-    _, e2e_value = aggregate_rate(sum(e2e_ms) / len(e2e_ms), flops, 1, world, dev)
+    e2e_value = None
+    if e2e_ms:
+        _, e2e_value = aggregate_rate(sum(e2e_ms) / len(e2e_ms), flops, 1, world, dev)
 
     if world > 1:
         dist.barrier()
@@ -431,7 +473,7 @@ def run_phobos(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": sum(e2e_ms) / len(e2e_ms),
-                "api": "phobos_sgemm_host (pinned host buffers)"},
+                "api": "phobos_sgemm_host (pinned host buffers)"} if e2e_ms else None,
         "gpu_launches": int(launches),
         "clocks": clk,
     }
@@ -443,6 +485,13 @@ def run_phobos(args):
 
 def main():
     args = parse_args()
+    _, world, _ = dist_env()
+    if args.multicast and (world > 1 or args.gpus > 1):
+        # TMA multicast is a one-GPU option (its tensor maps cover this GPU's
+        # own memory only): never part of a multi-GPU run.
+        print("bench.py: --multicast runs on one GPU only (WORLD_SIZE=%d, --gpus %d)"
+              % (world, args.gpus), file=sys.stderr, flush=True)
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_phobos(args)

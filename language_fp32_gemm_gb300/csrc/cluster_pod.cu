@@ -403,7 +403,10 @@ class Pod {
       return mark_issued(i, nullptr);
     }
     if (wait_deps(i, compute_) != PHOBOS_OK) return PHOBOS_ERR_CUDA;
-    // The step leaf: C += alpha * A_chunk * B_chunk (implicit beta = 1).
+    // The step leaf: C += alpha * A_chunk * B_chunk (implicit beta = 1).  Pods
+    // may run as ranks of a multi-GPU job, so leaves always take the automatic
+    // plan, which never turns on TMA multicast (and the library refuses a
+    // multicast plan in such a rank).
     const phobos_status_t st = phobos_sgemm_ex(ca.rows, ca.cols, kc, h_.alpha, a, kc, b, ca.cols, 1.0f, c,
                                                ca.cols, compute_, PHOBOS_MATH_DEFAULT, nullptr);
     if (st != PHOBOS_OK) return st;

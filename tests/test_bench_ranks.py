@@ -73,3 +73,18 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"] == {"value": d["value"], "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "sgemm_256"
+
+
+def test_multicast_refused_under_a_two_rank_launch():
+    # TMA multicast is a one-GPU option: bench.py launched as two ranks (the
+    # way a multi-GPU run is launched) must refuse --multicast before it
+    # touches a device or starts a process group.
+    import subprocess
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--gpus", "2",
+           "--steps", "1", "--warmup", "1", "--multicast"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode != 0
+    assert "--multicast runs on one GPU only" in out.stderr
+    assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
