@@ -110,7 +110,11 @@ typedef enum {
  *                  at once are launched (36 on GB300, i.e. 144 of the 152
  *                  SMs), so the planner leaves it off: measured against the
  *                  pair kernel it is 5 % slower at 8192^3, 10 % at 4096^3 and
- *                  even at 16384^3.
+ *                  even at 16384^3.  Multicast is a one-GPU option: its
+ *                  tensor maps cover this GPU's own memory only, and a plan
+ *                  with multicast = 1 is refused (PHOBOS_ERR_UNSUPPORTED)
+ *                  in a process that is one rank of a multi-process job
+ *                  (environment WORLD_SIZE or LOCAL_WORLD_SIZE above 1).
  *  super_m/_n      super-tile: the output tiles are walked super-tile by
  *                  super-tile (an L2-locality group on one GPU).
  *  super_k         K chunk of the cluster split: super_k < K runs an init
@@ -215,8 +219,9 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha,
                                   void *stream, phobos_math_t math);
 
 /*
- * Synchronize `stream`, then read and clear the device status word of the
- * current device.  PHOBOS_ERR_TIMEOUT if a kernel's bounded wait expired since
+ * Synchronize `stream`, then read and clear the device status words of the
+ * current device (the library's, and the no-allocation entry point's once it
+ * has run there).  PHOBOS_ERR_TIMEOUT if a kernel's bounded wait expired since
  * the last check, PHOBOS_ERR_CUDA if synchronization failed, else PHOBOS_OK.
  */
 phobos_status_t phobos_check_device(void *stream);
@@ -247,8 +252,11 @@ phobos_status_t phobos_release(void);
  * latency-critical loops that cannot take the implicit synchronisation and
  * latency of cudaMalloc/cudaFree.
  *
- * Same arguments, layout, ownership and result as phobos_sgemm_ex with
- * PHOBOS_MATH_3XTF32 and the automatic plan.  The call allocates nothing:
+ * Same arguments, layout and ownership as phobos_sgemm_ex with
+ * PHOBOS_MATH_3XTF32, and a result within the same 3xTF32 bound: the same
+ * operand split and TMEM partial lengths, but single-CTA tiles without the
+ * tail split, so the rounding order (not the accuracy) may differ from the
+ * automatic plan's.  The call allocates nothing:
  * no cudaMalloc, cudaMallocAsync, cudaFree or other allocating routine.  Its
  * scratch is one fixed device array inside the library
  * (PHOBOS_NOALLOC_SCRATCH_BYTES of split operands plus a status word).  Every
@@ -266,10 +274,11 @@ phobos_status_t phobos_release(void);
  *    every element a call reads, padding included.  Calls whose work overlaps
  *    on the GPU (for example on two streams at once) race on the array:
  *    serialise them.
- *  - Errors: as phobos_sgemm_ex.  An expired device-side wait is recorded in
- *    the array's status word.  It is reported as PHOBOS_ERR_TIMEOUT (and
- *    cleared) only when PHOBOS_DEBUG_SYNC=1, since that check synchronises
- *    the stream.
+ *  - Errors: as phobos_sgemm_ex, including PHOBOS_ERR_UNSUPPORTED when M, N
+ *    or K exceeds 2^31 - 1024.  An expired device-side wait is recorded in
+ *    the array's status word.  phobos_check_device reads and clears that word
+ *    beside the library's own; with PHOBOS_DEBUG_SYNC=1 every call also
+ *    synchronises and reports it as PHOBOS_ERR_TIMEOUT.
  */
 #define PHOBOS_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 phobos_status_t phobos_sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,

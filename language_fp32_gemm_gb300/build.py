@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libphobos_gemm.so")
 SOURCES = ["phobos_gemm.cu", "sgemm_tc.cu", "sgemm_ffma.cu", "split.cu", "noalloc.cu",
            "cluster_plan.cc", "cluster_pod.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "cluster_internal.h",
+HEADERS = ["ptx.cuh", "internal.h", "host_rules.h", "cluster_internal.h",
            os.path.join("..", "..", "include", "phobos_gemm.h"),
            os.path.join("..", "..", "include", "phobos_cluster.h")]
 

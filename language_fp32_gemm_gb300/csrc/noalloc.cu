@@ -22,6 +22,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "host_rules.h"
 #include "internal.h"
 
 namespace phobos {
@@ -30,8 +31,6 @@ namespace {
 constexpr size_t kHeadBytes = 256;  // status word, padded to keep the operands aligned
 constexpr size_t kScratchBytes = PHOBOS_NOALLOC_SCRATCH_BYTES;
 constexpr int kBM = 128, kBK = 32;
-// K blocks per TMEM partial sum, by K, as the allocating path chooses them.
-int promote_for(int64_t k) { return k <= 128 ? 1 : k <= 512 ? 2 : k <= 2048 ? 4 : 8; }
 constexpr int64_t kSuper = 4096;
 constexpr int kMaxDevices = 64;
 
@@ -112,6 +111,16 @@ size_t scratch_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 }  // namespace
+
+// The status word of the no-allocation entry point on device `dev`, or null
+// when that entry point has not run on the device yet; phobos_check_device
+// reads and clears it beside the library's own word.
+int *noalloc_status_word(int dev) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  return static_cast<int *>(g_scratch_addr[dev]);
+}
+
 }  // namespace phobos
 
 using namespace phobos;
@@ -123,6 +132,8 @@ extern "C" phobos_status_t phobos_sgemm_noalloc(int64_t M, int64_t N, int64_t K,
   if (M < 0 || N < 0 || K < 0) return PHOBOS_ERR_INVALID_VALUE;
   if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
     return PHOBOS_ERR_INVALID_VALUE;
+  // the same limit as every other entry point, before any size is narrowed to int
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return PHOBOS_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return PHOBOS_OK;
   if (!C) return PHOBOS_ERR_INVALID_VALUE;
   const bool products = K > 0 && alpha != 0.0f;
@@ -178,7 +189,7 @@ extern "C" phobos_status_t phobos_sgemm_noalloc(int64_t M, int64_t N, int64_t K,
       t.alpha = alpha;
       t.beta = beta;
       t.vec_c = (ldc % 4 == 0) && aligned16(C);
-      t.promote_blocks = promote_for(K);
+      t.promote_blocks = promote_blocks_for(K);  // the rule of every split-TF32 call
       t.sm_count = g_sm_count[dev];
       t.err = status_word;
       st = ok(launch_tc(t, 3, bn, tc_max_stages(3, bn), stream));

@@ -17,36 +17,16 @@
 #include <mutex>
 #include <utility>
 
+#include "host_rules.h"
 #include "internal.h"
 
 namespace phobos {
 namespace {
 
-constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;  // kernels index with int
 constexpr int kTcBK = 32;
 constexpr int kTcBM = 128;
 constexpr int64_t kFfmaMacLimit = int64_t{1} << 25;     // DEFAULT: FFMA up to 32 Mi MACs
 constexpr int64_t kDefaultSuper = 4096;                 // super-tile edge (raster group)
-// K blocks (of 32) summed in TMEM before the partial sum is added into fp32
-// registers with round-to-nearest adds, for split TF32.  The truncation error
-// of one partial is largest relative to sum|a||b| when the whole K spans few
-// partials.  Measured on GB300 (max over 4 M outputs, normal data, bar 2^-20 =
-// 9.5e-7):
-//   partials of 8 blocks: 1.07e-6 at K = 256, 4.9e-7 at K = 1024, 2.4e-7 at K = 4096
-//   partials of 4 blocks: 8.9e-7 at K = 128, 5.6e-7 at K = 256, 2.5e-7 at K = 1024
-//   partials of 2 blocks: 6.9e-7 at K = 64, 3.2e-7 at K = 256, 1.9e-7 at K = 512
-//   partials of 1 block:  3.7e-7 at K = 64, 2.4e-7 at K = 128
-// while shorter partials cost speed (8192^3: 367, 355, 322, 204 TFLOP/s).  So
-// the length follows K, keeping every case at 5e-7 or below.  Two partials
-// are also the slack the next tile's MMAs have while the accumulator warps
-// store a tile, so above K = 1024 the longer partials are used: 8 blocks
-// measured 4.7e-7 at K = 1025, 3.3e-7 at K = 2000 (2 M outputs each).
-int promote_blocks_for(int64_t k) {
-  if (k <= 128) return 1;
-  if (k <= 512) return 2;
-  if (k <= 1024) return 4;
-  return 8;
-}
 // Single TF32 (bound 2^-10) promotes every K = 1024.
 constexpr int kTf32PromoteBlocks = 32;
 // fp16 / bf16 inputs promote every 8 blocks of 64 (K = 512): a partial's
@@ -370,6 +350,16 @@ phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
   return PHOBOS_OK;
 }
 
+// True in a process launched as one rank of a multi-process (multi-GPU) job,
+// as torchrun and similar launchers announce it.
+bool in_multi_rank_job() {
+  for (const char *name : {"WORLD_SIZE", "LOCAL_WORLD_SIZE"}) {
+    const char *v = std::getenv(name);
+    if (v && std::atoll(v) > 1) return true;
+  }
+  return false;
+}
+
 phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
                               const phobos_gemm_plan_t &p) {
   if (math == PHOBOS_MATH_FFMA && p.path != PHOBOS_PATH_FFMA) return PHOBOS_ERR_INVALID_VALUE;
@@ -380,6 +370,8 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (math == PHOBOS_MATH_DEFAULT && half_path(p.path)) return PHOBOS_ERR_INVALID_VALUE;
   if (p.multicast != 0 && p.multicast != 1) return PHOBOS_ERR_INVALID_VALUE;
   const bool mc = p.multicast == 1;
+  // TMA multicast stays a one-GPU option: never in a rank of a multi-GPU job.
+  if (mc && in_multi_rank_job()) return PHOBOS_ERR_UNSUPPORTED;
   // multicast: two CTA pairs side by side along N (cluster 2 x 2), tf32 operands
   // split by the pre-pass
   if ((p.cluster_m != 1 && p.cluster_m != 2) || p.cluster_n != (mc ? 2 : 1))
@@ -878,9 +870,22 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, 
 phobos_status_t phobos_check_device(void *stream) {
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState *dev = nullptr;
-  phobos_status_t st = device_state(&dev, nullptr);
+  int device = 0;
+  phobos_status_t st = device_state(&dev, &device);
   if (st != PHOBOS_OK) return st;
-  return read_status_word(*dev, static_cast<cudaStream_t>(stream));
+  st = read_status_word(*dev, static_cast<cudaStream_t>(stream));
+  // The no-allocation entry point keeps its own word inside its fixed
+  // scratch; read and clear it too, so an expired wait there is reported here.
+  if (int *word = noalloc_status_word(device)) {
+    int v = 0;
+    if (cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
+    if (v != 0) {
+      if (cudaMemset(word, 0, sizeof(int)) != cudaSuccess) return PHOBOS_ERR_CUDA;
+      if (st == PHOBOS_OK) st = PHOBOS_ERR_TIMEOUT;
+    }
+  }
+  return st;
 }
 
 phobos_status_t phobos_set_timing_events(void *start, void *stop) {

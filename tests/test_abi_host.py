@@ -150,6 +150,51 @@ def test_multicast_plans_are_validated_before_any_device_call(lib):
                                   phobos.PHOBOS_MATH_3XTF32, single) == phobos.PHOBOS_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("var", ["WORLD_SIZE", "LOCAL_WORLD_SIZE"])
+def test_multicast_refused_in_a_rank_of_a_multi_gpu_job(lib, monkeypatch, var):
+    # TMA multicast is a one-GPU option: a process launched as one rank of a
+    # multi-process job gets PHOBOS_ERR_UNSUPPORTED for a valid multicast plan,
+    # before any device call; the same plan without multicast is not refused
+    # by that rule (it fails later here only for want of a GPU).
+    M = N = K = 1024
+    p = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
+    p.multicast, p.cluster_n = 1, 2
+    monkeypatch.setenv(var, "2")
+    st = phobos.phobos_sgemm_ex(M, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0,
+                                phobos.PHOBOS_MATH_3XTF32, p)
+    assert st == phobos.PHOBOS_ERR_UNSUPPORTED
+    monkeypatch.setenv(var, "1")
+    if var == "WORLD_SIZE":
+        monkeypatch.delenv("LOCAL_WORLD_SIZE", raising=False)
+    else:
+        monkeypatch.delenv("WORLD_SIZE", raising=False)
+    st = phobos.phobos_sgemm_ex(M, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0,
+                                phobos.PHOBOS_MATH_3XTF32, p)
+    assert st != phobos.PHOBOS_ERR_UNSUPPORTED
+
+
+def test_automatic_plans_never_choose_multicast(lib):
+    for shape in [(256, 256, 256), (4096, 4096, 4096), (8192, 8192, 8192),
+                  (3001, 5003, 1999), (65536, 256, 4096), (16384, 16384, 16384)]:
+        M, N, K = shape
+        for math in ("default", "3xtf32", "tf32", "fp16", "bf16", "ffma"):
+            p = phobos.phobos_gemm_plan(M, N, K, K, N, N, math)
+            assert p.multicast == 0 and p.cluster_n == 1
+
+
+def test_noalloc_refuses_dimensions_beyond_the_kernels_int_range(lib):
+    # Even with nothing to multiply (alpha = 0, then C = beta * C), M and N
+    # beyond 2^31 - 1024 are refused before any size is narrowed or any
+    # device call is made; C may then be any pointer.
+    big = 1 << 31
+    assert phobos.phobos_sgemm_noalloc(big, 4, 4, 0.0, 16, 4, 16, 4, 0.5, 16, 4, 0) == \
+        phobos.PHOBOS_ERR_UNSUPPORTED
+    assert phobos.phobos_sgemm_noalloc(4, big, 4, 0.0, 16, 4, 16, big, 0.5, 16, big, 0) == \
+        phobos.PHOBOS_ERR_UNSUPPORTED
+    assert phobos.phobos_sgemm_noalloc(4, 4, big, 1.0, 16, big, 16, 4, 0.5, 16, 4, 0) == \
+        phobos.PHOBOS_ERR_UNSUPPORTED
+
+
 def test_missing_library_raises_instead_of_falling_back():
     # No CPU fallback: without the built library every entry point raises.
     code = ("import language_fp32_gemm_gb300 as p\n"

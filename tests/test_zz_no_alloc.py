@@ -5,9 +5,9 @@ themselves: a serving process whose device memory its own allocator reserved
 up front (a new cudaMalloc could fail or fragment that pool), or a
 latency-critical loop that cannot take cudaMalloc/cudaFree's implicit
 synchronisation.  Its scratch is a fixed array inside the library, shared by
-every call.  These tests check that two calls in a row each give the allocating
-entry point's result, within the 3xTF32 tolerance, and that a problem too
-large for the fixed scratch is refused without touching C.
+every call.  These tests check that calls in a row each agree with the CPU
+oracle and with the allocating entry point, within the 3xTF32 tolerance, and
+that a problem too large for the fixed scratch is refused without touching C.
 
 This file is named to be collected last; it passes alone or after the others.
 """
@@ -40,11 +40,13 @@ def _noalloc(dA, dB, dC, alpha, beta, stream):
                                        dC.data_ptr(), N, stream)
 
 
-def test_two_calls_match_the_allocating_entry_point(dev):
+def test_calls_in_a_row_match_the_oracle_and_the_allocating_entry_point(dev):
     stream = torch.cuda.current_stream(dev).cuda_stream
-    # The second problem is smaller, so stale operands of the first call sit
-    # in the shared scratch around the second call's buffers.
-    for seed, (M, N, K) in ((61, (1000, 900, 700)), (62, (300, 260, 200))):
+    # Three calls in a row.  Each later problem is smaller than the first, so
+    # stale operands of earlier calls sit in the shared scratch around its
+    # buffers.  K = 2000 takes the 8-block TMEM partials of K above 1024.
+    for seed, (M, N, K) in ((61, (1000, 900, 700)), (63, (256, 256, 2000)),
+                            (62, (300, 260, 200))):
         A = si.normal(seed, 0, (M, K))
         B = si.normal(seed, 1, (K, N))
         C0 = si.uniform_pm1(seed, 2, (M, N))
@@ -58,11 +60,14 @@ def test_two_calls_match_the_allocating_entry_point(dev):
                                     c_alloc.data_ptr(), N, stream, phobos.PHOBOS_MATH_3XTF32)
         assert st == phobos.PHOBOS_OK, phobos.status_string(st)
         torch.cuda.synchronize()
-        got = c_noalloc.cpu().numpy().astype(np.float64)
+        # no expired wait in either entry point's status word
+        assert phobos.phobos_check_device(stream) == phobos.PHOBOS_OK
+        got = c_noalloc.cpu().numpy()
         want = c_alloc.cpu().numpy().astype(np.float64)
-        _, den = oracle.sgemm(A, B, C0, alpha, beta)
+        ref, den = oracle.sgemm(A, B, C0, alpha, beta)
         assert np.isfinite(got).all()
-        assert np.max(np.abs(got - want) / den) <= oracle.TOL_FP32
+        assert oracle.max_rel_error(got, ref, den) <= oracle.TOL_FP32, (M, N, K)
+        assert np.max(np.abs(got.astype(np.float64) - want) / den) <= oracle.TOL_FP32, (M, N, K)
 
 
 def test_too_large_for_the_scratch_is_refused(dev):
