@@ -17,3 +17,13 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+def pytest_terminal_summary(terminalreporter):
+    # The largest oracle error of each full-size workload run on the GPU.
+    mod = sys.modules.get("test_configs_gpu")
+    errors = getattr(mod, "MAX_ERRORS", None)
+    if errors:
+        terminalreporter.write_sep("-", "max |C - C_ref| / (|alpha| sum|a||b| + |beta||c_old|)")
+        for key, err in errors.items():
+            terminalreporter.write_line("%-60s %.3g" % (key, err))
