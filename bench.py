@@ -4,7 +4,8 @@
 Default workload: the 8192^3 fp32 SGEMM (A, B uniform[-1,1], C_old normal,
 alpha = 0.75, beta = 0.25, seed 2) through libphobos_gemm's default plan
 (split TF32 on the tcgen05 tensor cores).  One "step" is one full call: the
-operand pre-pass and the main kernel.
+split of A and B into tf32 pairs (by the main kernel itself for this shape)
+and the GEMM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--math M]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
@@ -468,7 +469,8 @@ def run_phobos(args):
                    "plan": plan.as_dict(), "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (%.0f MiB of A, B, C)"
                          % (4 * (M * K + K * N + M * N) / 2 ** 20),
-                   "step": "operand split pre-pass + main kernel, one call"},
+                   "step": "one library call: split of A and B into tf32 pairs (inside the "
+                           "main kernel, or a pre-pass, as the plan chooses) + the GEMM"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,

@@ -35,6 +35,8 @@
  *    PHOBOS_TEST_WITHHOLD_LOAD=1 makes the tensor-core kernel skip its first
  *    operand load: its wait on that load expires after about two seconds, the
  *    kernel stops without writing C, and the status word reports it.
+ *    PHOBOS_TEST_WITHHOLD_SPLIT=1 does the same through the in-kernel panel
+ *    split (a_split = 3): the first split item is never marked done.
  *  - Thread safety: calls may come from several host threads.  Calls that
  *    share one stream are ordered by it; calls on different streams use
  *    different workspaces.
@@ -138,14 +140,26 @@ typedef enum {
  *                  tail's K blocks dealt evenly to every CTA).  Every piece
  *                  spans at least K = 128.  Results are equal up to rounding
  *                  order and deterministic.
- *  a_split         tensor-core paths: where A is split into tf32 big/small
- *                  (0 = chosen per call: inside the kernel when N <= 1536 and
- *                  A's rows are 16-byte aligned, where a separate pass over A
- *                  would cost a large share of the GEMM; 1 = a pre-pass into
- *                  the workspace; 2 = inside the kernel, which needs
- *                  lda % 4 == 0 and a 16-byte-aligned A, else
- *                  PHOBOS_ERR_UNSUPPORTED).  Identical results either way.
- *                  FP16 and BF16 always convert A in the pre-pass (0 or 1).
+ *  a_split         tensor-core paths: where A (and B) are split into tf32
+ *                  big/small.
+ *                   0 = chosen per call: 2 when N <= 1536 and A's rows are
+ *                       16-byte aligned (a separate pass over A would cost a
+ *                       large share of the GEMM there), else 3 for split TF32
+ *                       with CTA pairs, else 1.
+ *                   1 = a pre-pass kernel splits A and B into the workspace
+ *                       before the GEMM kernel starts.
+ *                   2 = A is split in shared memory inside the GEMM kernel,
+ *                       B by the pre-pass; needs lda % 4 == 0 and a
+ *                       16-byte-aligned A, else PHOBOS_ERR_UNSUPPORTED.
+ *                   3 = the GEMM kernel splits A and B into the workspace
+ *                       itself, overlapped with its own tiles: two extra
+ *                       warps per CTA split the panels in the order the tiles
+ *                       first need them, and each CTA waits only for the
+ *                       panels of its current tile; tf32 CTA pairs without
+ *                       multicast only (else PHOBOS_ERR_UNSUPPORTED), any
+ *                       leading dimension and alignment.
+ *                  Identical results whichever is used.  FP16 and BF16 always
+ *                  convert A in the pre-pass (0 or 1).
  *  FP16 and BF16 plans run the tensor-core kernel with its deepest stage ring
  *  only (stages must equal the planner's value).
  */

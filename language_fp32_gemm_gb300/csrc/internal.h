@@ -80,7 +80,9 @@ struct TcArgs {
   int vec_c;
   int promote_blocks;  // K blocks per TMEM partial sum before it is added into registers
   int sm_count;        // SMs of the device: the persistent grid size
-  int withhold_first_load;  // testing only: skip the first operand load (a wait then expires)
+  // testing only: 1 = skip the first operand load, 2 = never publish the flag of
+  // the first in-kernel split item; either way a bounded wait then expires
+  int withhold_first_load;
   // Split of the last, partial wave along K.  Tiles [0, full_tiles) are
   // computed whole, strided over the workers (CTAs, or CTA pairs).  The K
   // blocks of the remaining tiles, laid end to end, are dealt evenly to
@@ -108,7 +110,35 @@ struct TcArgs {
   unsigned *flags;
   unsigned epoch;
   int *err;
+  // In-kernel panel split (CTA pairs, tf32 operands).  1: warps 10 and 11 of
+  // every CTA split the caller's raw A (and B when split_b) into the
+  // workspace buffers that the operand maps cover, while the GEMM runs: an
+  // item is one 32-row slice of a 256-row A panel, or one 32-column slice of
+  // a 256-column B panel (written transposed, K-major), over a K chunk of
+  // kSplitChunkBlocks k blocks of this launch, padding written as zeros.
+  // Items are claimed from the counter split_next[epoch - 1] in the order the
+  // persistent tiles first need them (by wave, then K chunk); each publishes
+  // `epoch` in its flag once its stores are visible:
+  //   A: split_flags[(tm * KC + kc) * 8 + slice]
+  //   B: split_flags[((tiles_m + tn) * KC + kc) * 8 + slice]
+  // with KC = ceil(k_blocks / kSplitChunkBlocks).  A CTA's producer waits for
+  // the four flags of its 128 rows of A and 128 rows of B (transposed) at
+  // the start of every K chunk of a tile.  The host zeroes flags and counters
+  // before each call.
+  int split_inline, split_b;
+  const float *A_raw, *B_raw;
+  int64_t lda, ldb;
+  int K;   // K of the whole problem: the raw operands' extent
+  int kp;  // row length of the workspace operand buffers (K rounded up to 32)
+  float *a_big, *a_small, *b_big, *b_small;
+  int vec_a, vec_b;  // 16-byte loads of the raw operands allowed
+  unsigned *split_flags;
+  unsigned *split_next;
 };
+// K blocks per item of the in-kernel panel split (256 of K).  Measured on
+// GB300: items of 64 of K spent more time in their flag fences and round trips
+// than they saved at the start (4096^3: 0.542 against 0.447 ms per call).
+constexpr int kSplitChunkBlocks = 8;
 // Operand types of the tensor-core kernel: tf32 from fp32 containers (one or
 // three passes), or pre-converted fp16 / bf16 (one pass, MMA kind::f16).
 enum TcKind : int { kTcTf32 = 0, kTcF16 = 1, kTcBf16 = 2 };

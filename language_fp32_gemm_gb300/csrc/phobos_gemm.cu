@@ -381,7 +381,11 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
     return PHOBOS_ERR_UNSUPPORTED;
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
   if (p.tail_split < 0 || p.tail_split > kMaxTailSplit) return PHOBOS_ERR_INVALID_VALUE;
-  if (p.a_split < 0 || p.a_split > 2) return PHOBOS_ERR_INVALID_VALUE;
+  if (p.a_split < 0 || p.a_split > 3) return PHOBOS_ERR_INVALID_VALUE;
+  // the in-kernel panel split runs in tf32 CTA pairs without multicast
+  if (p.a_split == 3 && (p.cluster_m != 2 || mc ||
+                         (p.path != PHOBOS_PATH_TF32 && p.path != PHOBOS_PATH_3XTF32)))
+    return PHOBOS_ERR_UNSUPPORTED;
   if (p.path == PHOBOS_PATH_FFMA) {
     if (p.cluster_m != 1) return PHOBOS_ERR_UNSUPPORTED;
     if (!((p.tile_m == 128 && p.tile_n == 128) || (p.tile_m == 64 && p.tile_n == 64)))
@@ -396,7 +400,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
       return PHOBOS_ERR_INVALID_VALUE;
     const int max_st = pair ? tc_pair_max_stages(passes, p.tile_n) : tc_max_stages(passes, p.tile_n);
     if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
-    if ((p.a_split == 2 || mc) && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
+    if ((p.a_split >= 2 || mc) && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
     // 16-bit inputs: pre-converted A, deepest ring
     if (half_path(p.path) && (p.a_split == 2 || (p.stages != max_st && p.stages != 4)))
       return PHOBOS_ERR_INVALID_VALUE;
@@ -490,15 +494,19 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   // or by the pre-pass into the workspace.  16-bit inputs are always
   // converted by the pre-pass.
   const bool a_tma_ok = (lda % 4 == 0) && aligned16(A);
-  bool a_inline = false;
+  const int max_st = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
+  bool a_inline = false;      // A split in shared memory, B by the pre-pass
+  bool split_inline = false;  // A and B split into the workspace by the GEMM kernel itself
   if (half) {
-    if (p.a_split == 2) return PHOBOS_ERR_UNSUPPORTED;
+    if (p.a_split >= 2) return PHOBOS_ERR_UNSUPPORTED;
   } else if (p.a_split == 2) {
     if (!a_tma_ok) return PHOBOS_ERR_UNSUPPORTED;
     a_inline = true;
-  } else if (p.a_split == 0 && !mc) {
-    const int max_st = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
-    a_inline = a_tma_ok && N <= kInlineSplitMaxN && p.stages == max_st;
+  } else if (p.a_split == 3) {
+    split_inline = true;  // validated: tf32 CTA pairs, no multicast, deepest ring
+  } else if (p.a_split == 0 && !mc && p.stages == max_st) {
+    a_inline = a_tma_ok && N <= kInlineSplitMaxN;
+    split_inline = !a_inline && pair && passes == 3;
   }
   const int64_t a_bytes = round_up(Mp * Kp * elem, 256), b_bytes = round_up(Np * Kp * elem, 256);
   const int ops = passes == 3 ? 2 : 1;  // big (+ small)
@@ -529,7 +537,15 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int full_tiles = tail_units > 0 ? total_tiles - tail : total_tiles;
   const int64_t slots = static_cast<int64_t>(tail_units) * (mc ? 2 : 1);  // one partial sum per pair at most
   const size_t part_bytes = static_cast<size_t>(round_up(slots * bm * bn * 4, 256));
-  const size_t flag_bytes = static_cast<size_t>(round_up(slots * 2 * kEpiWarps * 4, 256));
+  // flags: the tail split's, then (in-kernel panel split) one per item of the
+  // longest launch and one item counter per launch
+  const int64_t tail_flags = slots * 2 * kEpiWarps;
+  const int64_t chunk_kc = (chunk_blocks_max + kSplitChunkBlocks - 1) / kSplitChunkBlocks;
+  const int64_t launches = p.super_k < K ? (Kp / bk + chunk_blocks_max - 1) / chunk_blocks_max : 1;
+  const int64_t split_flags = split_inline ? (Mp / bm + Np / bn) * chunk_kc * 8 : 0;
+  const int64_t split_counters = split_inline ? launches : 0;
+  const size_t flag_bytes =
+      static_cast<size_t>(round_up((tail_flags + split_flags + split_counters) * 4, 256));
   const size_t need = ops_bytes + part_bytes + flag_bytes;
   Buffer &ws = g_workspaces[{device, reinterpret_cast<uintptr_t>(stream)}];
   void *const old_ws = ws.ptr;
@@ -548,8 +564,11 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   float *a_small = passes == 3 ? reinterpret_cast<float *>(base + ops * b_bytes + a_bytes) : nullptr;
 
   // Flags must not hold a value a launch of this call will wait for: the
-  // split-TF32 / TF32 pre-pass zeroes them in the same launch.
-  if (half) {
+  // split-TF32 / TF32 pre-pass zeroes them in the same launch; without a
+  // pre-pass a memset does.
+  if (split_inline) {
+    if (cudaMemsetAsync(flags, 0, flag_bytes, stream) != cudaSuccess) return PHOBOS_ERR_CUDA;
+  } else if (half) {
     if (flag_bytes && cudaMemsetAsync(flags, 0, flag_bytes, stream) != cudaSuccess)
       return PHOBOS_ERR_CUDA;
     st = cuda_status(counted(launch_convert_rows(A, lda, static_cast<int>(M), static_cast<int>(K),
@@ -580,7 +599,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     sa.b_big = b_big;
     sa.b_small = b_small;
     sa.flags = flags;
-    sa.n_flags = static_cast<int64_t>(flag_bytes / 4);
+    sa.n_flags = tail_flags;
     st = cuda_status(counted(launch_split_ab(sa, a_inline ? 0 : 1, reuse_b ? 0 : 1, stream)));
     if (st != PHOBOS_OK) return st;
   }
@@ -607,6 +626,24 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     return st;
   t.a_inline = a_inline ? 1 : 0;
   t.multicast = mc ? 1 : 0;
+  if (split_inline) {
+    t.split_inline = 1;
+    t.split_b = reuse_b ? 0 : 1;  // a reused B was split by an earlier call on this stream
+    t.A_raw = A;
+    t.B_raw = B;
+    t.lda = lda;
+    t.ldb = ldb;
+    t.K = static_cast<int>(K);
+    t.kp = static_cast<int>(Kp);
+    t.a_big = a_big;
+    t.a_small = a_small;
+    t.b_big = b_big;
+    t.b_small = b_small;
+    t.vec_a = a_tma_ok ? 1 : 0;
+    t.vec_b = (ldb % 4 == 0) && aligned16(B) ? 1 : 0;
+    t.split_flags = flags + tail_flags;
+    t.split_next = flags + tail_flags + split_flags;
+  }
   t.C = C;
   t.ldc = ldc;
   t.M = static_cast<int>(M);
@@ -623,7 +660,9 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
                      : half      ? kHalfPromoteBlocks
                                  : kTf32PromoteBlocks;
   t.sm_count = dev.sm_count;
-  t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD") ? 1 : 0;
+  t.withhold_first_load = env_flag("PHOBOS_TEST_WITHHOLD_LOAD")    ? 1
+                          : env_flag("PHOBOS_TEST_WITHHOLD_SPLIT") ? 2
+                                                                   : 0;
   t.full_tiles = full_tiles;
   t.tail_units = tail_units;
   // whole tiles stride over all SMs (pairs); with no whole tiles, only the

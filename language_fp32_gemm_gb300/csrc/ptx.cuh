@@ -16,6 +16,7 @@ enum : int {
   kDevTimeoutEpilogue = 0x103,
   kDevTimeoutDrain = 0x104,
   kDevTimeoutPartial = 0x105,
+  kDevTimeoutSplit = 0x106,  // a producer's wait for split operand panels
 };
 
 // A wait gives up after this much wall time (nanoseconds, %globaltimer).
@@ -448,6 +449,25 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *addr) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
   return v;
+}
+
+// Relaxed load at GPU scope: several of them may be in flight at once; a
+// fence_acq_rel_gpu after the last one gives them acquire semantics.
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *addr) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Order this thread's generic-proxy accesses of global memory with its later
+// (or, on the writing side, other threads' later) async-proxy accesses: TMA
+// loads of data written by ordinary stores.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ------------------------------------------------------------------- convert

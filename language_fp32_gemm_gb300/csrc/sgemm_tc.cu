@@ -191,13 +191,291 @@ struct RawAPrefetch {
   }
 };
 
+// ------------------------------------------------- in-kernel panel split
+// The order in which the splitter warps take the items of the split (see
+// TcArgs::split_inline): by the wave of the persistent walk that first needs a
+// panel, then by K chunk, then by panel and slice.  Wave v holds tiles
+// [v * units, (v + 1) * units) of the raster walk; the panels first needed in
+// wave v are those not needed by an earlier tile.
+struct SplitOrder {
+  int units, total, group_m, per_group, rows0, tiles_m, tiles_n, kc_n, waves;
+  bool with_b;
+  long long items;
+
+  __device__ __forceinline__ void init(const TcArgs &p, int units_) {
+    units = units_;
+    total = p.tiles_m * p.tiles_n;
+    group_m = p.group_m;
+    per_group = p.group_m * p.tiles_n;
+    rows0 = min(p.group_m, p.tiles_m);
+    tiles_m = p.tiles_m;
+    tiles_n = p.tiles_n;
+    kc_n = (p.k_blocks + kSplitChunkBlocks - 1) / kSplitChunkBlocks;
+    waves = (total + units - 1) / units;
+    with_b = p.split_b != 0;
+    items = static_cast<long long>(kc_n) * 8 * (tiles_m + (with_b ? tiles_n : 0));
+  }
+  // A panels (tile rows) first needed by a tile of index < t: in group g the
+  // walk visits rows first .. first + rows - 1 in its first column.
+  __device__ __forceinline__ int a_count(long long t) const {
+    if (t >= total) return tiles_m;
+    const int g = static_cast<int>(t / per_group);
+    const int r = static_cast<int>(t - static_cast<long long>(g) * per_group);
+    const int first = g * group_m;
+    return first + min(r, min(group_m, tiles_m - first));
+  }
+  // B panels (tile columns) first needed by a tile of index < t: column tn
+  // first appears at tile tn * rows0 of the first group.
+  __device__ __forceinline__ int b_count(long long t) const {
+    if (!with_b) return 0;
+    if (t >= total) return tiles_n;
+    return static_cast<int>(min(static_cast<long long>(tiles_n), (t + rows0 - 1) / rows0));
+  }
+  __device__ __forceinline__ long long base(int v) const {
+    const long long t = static_cast<long long>(v) * units;
+    return static_cast<long long>(kc_n) * 8 * (a_count(t) + b_count(t));
+  }
+  // Item i -> wave, operand (0 = A, 1 = B), panel, K chunk and 32-wide slice.
+  __device__ __forceinline__ void item(long long i, int &wave, int &is_b, int &panel, int &kc,
+                                       int &slice) const {
+    int lo = 0, hi = waves;  // base(lo) <= i < base(hi) = items
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (base(mid) <= i) lo = mid;
+      else hi = mid;
+    }
+    wave = lo;
+    const long long t0 = static_cast<long long>(lo) * units, t1 = t0 + units;
+    const int a0 = a_count(t0), a1 = a_count(t1), b0 = b_count(t0), b1 = b_count(t1);
+    const int per_kc = 8 * ((a1 - a0) + (b1 - b0));
+    const long long o = i - base(lo);
+    kc = static_cast<int>(o / per_kc);
+    const int rem = static_cast<int>(o - static_cast<long long>(kc) * per_kc);
+    const int pi = rem >> 3;
+    slice = rem & 7;
+    if (pi < a1 - a0) {
+      is_b = 0;
+      panel = a0 + pi;
+    } else {
+      is_b = 1;
+      panel = b0 + (pi - (a1 - a0));
+    }
+  }
+};
+
+// x -> tf32 pair: big = rna_tf32(x), small = rna_tf32(x - big) (exact difference).
+__device__ __forceinline__ void split4(const float4 &x, float4 &big, float4 &small) {
+  big.x = tf32_rna_bits(x.x); small.x = tf32_rna_bits(x.x - big.x);
+  big.y = tf32_rna_bits(x.y); small.y = tf32_rna_bits(x.y - big.y);
+  big.z = tf32_rna_bits(x.z); small.z = tf32_rna_bits(x.z - big.z);
+  big.w = tf32_rna_bits(x.w); small.w = tf32_rna_bits(x.w - big.w);
+}
+
+// Up to four elements x[k .. k+3] of a row of the caller's matrix (zeros at
+// and beyond `k_end`), as one 16-byte load when `vec` allows.
+__device__ __forceinline__ float4 load_row4(const float *row, int k, int k_end, bool vec) {
+  float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (vec && k + 3 < k_end) return __ldg(reinterpret_cast<const float4 *>(row + k));
+  if (k < k_end) x.x = __ldg(row + k);
+  if (k + 1 < k_end) x.y = __ldg(row + k + 1);
+  if (k + 2 < k_end) x.z = __ldg(row + k + 2);
+  if (k + 3 < k_end) x.w = __ldg(row + k + 3);
+  return x;
+}
+
+// Loads in flight per lane of a splitter warp: the items are latency-bound
+// (two warps per SM), so each lane issues this many 16-byte loads before it
+// uses the first.  32 made the items slower on GB300 (the 128 registers of
+// data no longer fit beside the rest of the kernel's 168).
+constexpr int kSplitLoads = 16;
+
+// One A item: rows r0 .. r0+31 over K [k0, k1) into the K-major workspace
+// rows (zeros past M and K).  Element e of the item is (row e / G, float4
+// group e % G), G = the item's float4 groups per row: each load and store
+// instruction of the warp covers whole 128-byte row segments.
+template <int PASSES>
+__device__ __forceinline__ void split_a_item(const TcArgs &p, int r0, int k0, int k1, int lane) {
+  constexpr int kGroups = kSplitChunkBlocks * kBK / 4;  // float4 groups per row of a whole item
+  const int groups = (k1 - k0) >> 2;                    // ... of this item (K tail: fewer)
+  constexpr int kBatches = 32 * kGroups / 32 / kSplitLoads;
+  static_assert(kBatches >= 1 && 32 * kGroups == 32 * kBatches * kSplitLoads, "whole batches");
+#pragma unroll 1
+  for (int b = 0; b < kBatches; ++b) {
+    float4 x[kSplitLoads];
+#pragma unroll
+    for (int j = 0; j < kSplitLoads; ++j) {
+      const int e = (b * kSplitLoads + j) * 32 + lane;
+      const int row = r0 + e / kGroups, c = e % kGroups;
+      x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < groups && row < p.M)
+        x[j] = load_row4(p.A_raw + static_cast<int64_t>(row) * p.lda, k0 + 4 * c, p.K, p.vec_a);
+    }
+#pragma unroll
+    for (int j = 0; j < kSplitLoads; ++j) {
+      const int e = (b * kSplitLoads + j) * 32 + lane;
+      const int row = r0 + e / kGroups, c = e % kGroups;
+      if (c < groups) {
+        float4 big, small;
+        split4(x[j], big, small);
+        const int64_t o = static_cast<int64_t>(row) * p.kp + k0 + 4 * c;
+        *reinterpret_cast<float4 *>(p.a_big + o) = big;
+        if (PASSES == 3) *reinterpret_cast<float4 *>(p.a_small + o) = small;
+      }
+    }
+  }
+}
+
+// One B item: columns n0 .. n0+31 of B over K [k0, k1), written transposed
+// (row n of the workspace holds column n of B).  Lane (c, q) = (lane % 8,
+// lane / 8) loads rows k = 8q .. 8q+7 of a 32-deep K block at columns
+// n0 + 4c .. +3 (each load instruction covers four 128-byte row segments),
+// so it holds an 8 x 4 block and writes each of its four columns as 32
+// contiguous bytes of K; the lanes of one q together cover 128 bytes of a
+// workspace row.  kSplitLoads / 8 K blocks are in flight at once.
+template <int PASSES>
+__device__ __forceinline__ void split_b_item(const TcArgs &p, int n0, int k0, int k1, int lane) {
+  const int c = lane & 7, q = lane >> 3;
+  const int n = n0 + 4 * c;
+  const bool vec = p.vec_b && n + 3 < p.N;
+  constexpr int kBlocks = kSplitLoads / 8;  // 32-deep K blocks per batch
+#pragma unroll 1
+  for (int kr = k0; kr < k1; kr += 32 * kBlocks) {
+    float4 x[kSplitLoads];
+#pragma unroll
+    for (int j = 0; j < kSplitLoads; ++j) {
+      const int k = kr + 32 * (j >> 3) + 8 * q + (j & 7);
+      x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k < k1 && k < p.K) {
+        const float *src = p.B_raw + static_cast<int64_t>(k) * p.ldb;
+        if (vec) {
+          x[j] = __ldg(reinterpret_cast<const float4 *>(src + n));
+        } else {
+          if (n < p.N) x[j].x = __ldg(src + n);
+          if (n + 1 < p.N) x[j].y = __ldg(src + n + 1);
+          if (n + 2 < p.N) x[j].z = __ldg(src + n + 2);
+          if (n + 3 < p.N) x[j].w = __ldg(src + n + 3);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kBlocks; ++h) {
+      const int kb = kr + 32 * h + 8 * q;
+      if (kr + 32 * h >= k1) break;  // k1 - k0 is a multiple of 32
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        // column n + t of the 8 x 4 block: K kb .. kb+7
+        auto col = [&](int i) {
+          const float4 &v = x[8 * h + i];
+          return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w;
+        };
+        float4 big0, small0, big1, small1;
+        split4(make_float4(col(0), col(1), col(2), col(3)), big0, small0);
+        split4(make_float4(col(4), col(5), col(6), col(7)), big1, small1);
+        const int64_t o = static_cast<int64_t>(n + t) * p.kp + kb;
+        *reinterpret_cast<float4 *>(p.b_big + o) = big0;
+        *reinterpret_cast<float4 *>(p.b_big + o + 4) = big1;
+        if (PASSES == 3) {
+          *reinterpret_cast<float4 *>(p.b_small + o) = small0;
+          *reinterpret_cast<float4 *>(p.b_small + o + 4) = small1;
+        }
+      }
+    }
+  }
+}
+
+// Splits item i and publishes its flag (every lane of the warp takes part).
+template <int PASSES>
+__device__ __forceinline__ void split_item(const TcArgs &p, const SplitOrder &ord, long long i,
+                                           int lane) {
+  int wave, is_b, panel, kc, slice;
+  ord.item(i, wave, is_b, panel, kc, slice);
+  const int kb0 = kc * kSplitChunkBlocks;
+  const int kb1 = min(p.k_blocks, kb0 + kSplitChunkBlocks);
+  const int k0 = (p.k_block0 + kb0) * kBK, k1 = (p.k_block0 + kb1) * kBK;
+  if (is_b)
+    split_b_item<PASSES>(p, panel * 256 + slice * 32, k0, k1, lane);
+  else
+    split_a_item<PASSES>(p, panel * 256 + slice * 32, k0, k1, lane);
+  // Every lane's stores visible (to the TMA's async proxy too), then the flag.
+  __threadfence();
+  fence_proxy_async_global();
+  __syncwarp();
+  // (failure-detection test: the first item's flag is never published, so a
+  // producer's bounded wait for it expires and the kernel aborts)
+  if (lane == 0 && !(p.withhold_first_load == 2 && i == 0)) {
+    const long long f =
+        (static_cast<long long>(is_b ? ord.tiles_m + panel : panel) * ord.kc_n + kc) * 8 + slice;
+    st_release_gpu(p.split_flags + f, p.epoch);
+  }
+}
+
+// Splitter warp: claims items in order, splits each, publishes its flag.
+// Never waits on another role, so the producers that wait on its flags always
+// make progress; stops early only when the CTA aborts.
+template <int PASSES>
+__device__ void run_splitter(const TcArgs &p, int units, int lane, volatile int *abort_flag) {
+  SplitOrder ord;
+  ord.init(p, units);
+  unsigned *next = p.split_next + (p.epoch - 1);
+  long long i = 0;
+  if (lane == 0) i = atomicAdd(next, 1u);
+  i = __shfl_sync(0xffffffffu, i, 0);
+  while (i < ord.items && !*abort_flag) {
+    // claim the following item now, so that the atomic's round trip overlaps
+    // this item's loads
+    unsigned claimed = 0;
+    if (lane == 0) claimed = atomicAdd(next, 1u);
+    split_item<PASSES>(p, ord, i, lane);
+    i = __shfl_sync(0xffffffffu, static_cast<long long>(claimed), 0);
+  }
+}
+
+// Producer side: wait until the four A slices and four B slices that this
+// CTA loads for K chunk kc of tile (tm, tn) are split.  Bounded like every
+// wait of the kernel.
+__device__ __forceinline__ bool wait_split_chunk(const TcArgs &p, int tm, int tn, int kc,
+                                                 uint32_t rank, volatile int *abort_flag) {
+  const int kc_n = (p.k_blocks + kSplitChunkBlocks - 1) / kSplitChunkBlocks;
+  const unsigned *fa = p.split_flags + (static_cast<long long>(tm) * kc_n + kc) * 8 + 4 * rank;
+  const unsigned *fb =
+      p.split_flags + (static_cast<long long>(p.tiles_m + tn) * kc_n + kc) * 8 + 4 * rank;
+  const unsigned e = p.epoch;
+  auto ready = [&]() {
+    const unsigned a0 = ld_relaxed_gpu(fa), a1 = ld_relaxed_gpu(fa + 1);
+    const unsigned a2 = ld_relaxed_gpu(fa + 2), a3 = ld_relaxed_gpu(fa + 3);
+    bool ok = a0 == e && a1 == e && a2 == e && a3 == e;
+    if (p.split_b) {
+      const unsigned b0 = ld_relaxed_gpu(fb), b1 = ld_relaxed_gpu(fb + 1);
+      const unsigned b2 = ld_relaxed_gpu(fb + 2), b3 = ld_relaxed_gpu(fb + 3);
+      ok = ok && b0 == e && b1 == e && b2 == e && b3 == e;
+    }
+    return ok;
+  };
+  if (!ready()) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t polls = 1; !ready(); ++polls) {
+      if (*abort_flag) return false;
+      if (polls >= kWaitLimitPolls || globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(p.err, 0, kDevTimeoutSplit);
+        return false;
+      }
+    }
+  }
+  fence_acq_rel_gpu();         // the flags' acquire: the split stores happen-before
+  fence_proxy_async_global();  // ... the TMA loads issued after this
+  return true;
+}
+
 template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32,
-          bool MC = false>
-__global__ void __launch_bounds__(threads_for(ASPLIT), 1)
+          bool MC = false, bool INL = false>
+__global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
     sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(KIND == kTcTf32 || (PASSES == 1 && !ASPLIT), "16-bit inputs: one pass, pre-converted");
   static_assert(!MC || (PAIR && !ASPLIT && KIND == kTcTf32), "multicast: pre-split tf32 pairs");
+  static_assert(!INL || (PAIR && !ASPLIT && !MC && KIND == kTcTf32),
+                "in-kernel panel split: tf32 CTA pairs without multicast");
   static_assert((4 * STAGES + 5) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit 256 bytes");
   // K elements per 128-byte stage row: 32 fp32/tf32 or 64 fp16/bf16.
   constexpr int kBKE = KIND == kTcTf32 ? kBK : 2 * kBK;
@@ -309,7 +587,12 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp >= 2 + kEpiWarps) {
+  if (INL && warp >= 2 + kEpiWarps) {
+    // ------------------------------- panel splitters (in-kernel panel split)
+    // Split the caller's A and B into the workspace, item by item, ahead of
+    // every CTA's producer (see TcArgs::split_inline).
+    run_splitter<PASSES>(p, units, lane, abort_flag);
+  } else if (ASPLIT && warp >= 2 + kEpiWarps) {
     // --------------------------------------- A-split warps (in-kernel split)
     // Each of the two warps converts half of every landed raw A tile in place:
     // big = rna_tf32(x) over x, small = rna_tf32(x - big) into the second A slot
@@ -324,7 +607,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
       for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
         const int s = g % STAGES;
         const uint32_t ph = (g / STAGES) & 1u;
-        if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+        if (p.withhold_first_load == 1 && g == 0) continue;  // failure-detection test
         if (!bounded_wait(a_full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutProducer)) {
           abort_peer();
           ok = false;
@@ -380,7 +663,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1u;
-          if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+          if (p.withhold_first_load == 1 && g == 0) continue;  // failure-detection test
           if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
             abort_peer();
             ok = false;
@@ -440,9 +723,17 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1u;
+          // In-kernel panel split: this CTA's rows of A and B for the K chunk
+          // starting here must have been split into the workspace.
+          if (INL && (kb == u.k_lo || kb % kSplitChunkBlocks == 0) &&
+              !wait_split_chunk(p, tm, tn, kb / kSplitChunkBlocks, rank, abort_flag)) {
+            abort_peer();
+            ok = false;
+            break;
+          }
           // Failure-detection test: the first stage is never loaded, so the
           // MMA issuer's bounded wait on it expires and the kernel aborts.
-          if (p.withhold_first_load && g == 0) continue;
+          if (p.withhold_first_load == 1 && g == 0) continue;
           if (!bounded_wait(empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutProducer)) {
             abort_peer();
             ok = false;
@@ -614,7 +905,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
         for (int kb = u.k_lo; kb < u.k_hi; ++kb, ++g) {
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1u;
-          if (p.withhold_first_load && g == 0) continue;  // failure-detection test
+          if (p.withhold_first_load == 1 && g == 0) continue;  // failure-detection test
           if (!bounded_wait(conv0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutProducer)) {
             abort_peer();
             ok = false;
@@ -896,14 +1187,15 @@ __global__ void __launch_bounds__(threads_for(ASPLIT), 1)
 
 // Launch configuration of one kernel instance: the persistent grid of `units`
 // CTAs, CTA pairs, or (multicast) clusters of two pairs.
-template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND, bool MC>
+template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND, bool MC,
+          bool INL = false>
 void tc_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, unsigned units,
                cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
   const unsigned ctas = MC ? 4u : PAIR ? 2u : 1u;
   cfg = {};
   cfg.gridDim = dim3(ctas * units, 1, 1);
-  cfg.blockDim = dim3(threads_for(ASPLIT), 1, 1);
+  cfg.blockDim = dim3(threads_for(ASPLIT || INL), 1, 1);
   cfg.dynamicSmemBytes = S::smem_bytes(STAGES);
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -915,11 +1207,11 @@ void tc_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, unsigned unit
 }
 
 template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32,
-          bool MC = false>
+          bool MC = false, bool INL = false>
 cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
-  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC>;
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC, INL>;
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -931,12 +1223,12 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
                              : static_cast<unsigned>(tiles < workers ? tiles : workers);
   if (units == 0) return cudaErrorInvalidValue;
   if (!PAIR) {
-    kern<<<units, threads_for(ASPLIT), smem, stream>>>(a);
+    kern<<<units, threads_for(ASPLIT || INL), smem, stream>>>(a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  tc_config<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC>(cfg, attr, units, stream);
+  tc_config<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC, INL>(cfg, attr, units, stream);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
@@ -967,7 +1259,7 @@ cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream, int 
   constexpr int kTop = kMax >= 6 ? 6 : kMax;
   // 16-bit inputs: one pass, pre-converted operands, the deepest ring only.
   if (kind != kTcTf32) {
-    if (PASSES != 1 || a.a_inline) return cudaErrorInvalidValue;
+    if (PASSES != 1 || a.a_inline || a.split_inline) return cudaErrorInvalidValue;
     if (stages == kTop)
       return kind == kTcF16 ? launch_one<BN, 1, kTop, PAIR, false, kTcF16>(a, stream)
                             : launch_one<BN, 1, kTop, PAIR, false, kTcBf16>(a, stream);
@@ -979,8 +1271,16 @@ cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream, int 
   // Multicast clusters: pre-split operands, the deepest ring.
   if (a.multicast) {
     if constexpr (PAIR) {
-      if (a.a_inline || stages != kTop) return cudaErrorInvalidValue;
+      if (a.a_inline || a.split_inline || stages != kTop) return cudaErrorInvalidValue;
       return launch_one<BN, PASSES, kTop, true, false, kTcTf32, true>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
+  // In-kernel panel split (CTA pairs): the deepest ring.
+  if (a.split_inline) {
+    if constexpr (PAIR) {
+      if (a.a_inline || stages != kTop) return cudaErrorInvalidValue;
+      return launch_one<BN, PASSES, kTop, true, false, kTcTf32, false, true>(a, stream);
     }
     return cudaErrorInvalidValue;
   }

@@ -4,7 +4,9 @@ Every mbarrier wait in the tensor-core kernel is bounded (about two seconds);
 when one expires the kernel records where in a device status word, stops all
 of its roles (in every CTA of a pair or multicast cluster), releases its
 tensor memory and returns.  PHOBOS_TEST_WITHHOLD_LOAD=1 makes the producer
-skip the first operand load, so the MMA issuer's wait for it runs out.  The
+skip the first operand load, so the MMA issuer's wait for it runs out;
+PHOBOS_TEST_WITHHOLD_SPLIT=1 makes the in-kernel panel split never publish its
+first item, so the producer's wait for that panel runs out.  The
 test checks that the host reads PHOBOS_ERR_TIMEOUT and that the context stays
 usable: the next call is correct.  Nothing here faults, traps or hangs the
 GPU.
@@ -31,24 +33,30 @@ def dev():
     return d
 
 
-@pytest.mark.parametrize("shape,multicast", [((128, 256, 96), 0), ((256, 256, 96), 0),
-                                             ((256, 512, 96), 1)],
-                         ids=["single_cta", "cta_pair", "multicast_cluster"])
-def test_expired_wait_is_reported_and_context_survives(dev, shape, multicast, monkeypatch):
+@pytest.mark.parametrize("shape,multicast,a_split,withhold", [
+    ((128, 256, 96), 0, 0, "LOAD"), ((256, 256, 96), 0, 0, "LOAD"), ((256, 512, 96), 1, 0, "LOAD"),
+    ((256, 256, 96), 0, 3, "LOAD"), ((256, 256, 96), 0, 3, "SPLIT")],
+    ids=["single_cta", "cta_pair", "multicast_cluster", "panel_split", "panel_split_flag"])
+def test_expired_wait_is_reported_and_context_survives(dev, shape, multicast, a_split, withhold,
+                                                       monkeypatch):
+    # withhold = LOAD: the producer skips its first operand load and the MMA
+    # issuer's wait expires; SPLIT (in-kernel panel split): the splitter never
+    # publishes its first item's flag and the producer's wait for it expires.
     M, N, K = shape
     plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
     assert plan.cluster_m == (2 if M > 128 else 1)
     if multicast:  # two CTA pairs sharing A through TMA multicast
         plan.multicast, plan.cluster_n = 1, 2
+    plan.a_split = a_split  # 3: A and B split by the GEMM kernel's splitter warps
     A = si.normal(71, 0, (M, K))
     B = si.normal(71, 1, (K, N))
     dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
     dC = torch.full((M, N), 5.0, device=dev)
     assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK  # nothing pending
-    monkeypatch.setenv("PHOBOS_TEST_WITHHOLD_LOAD", "1")
+    monkeypatch.setenv("PHOBOS_TEST_WITHHOLD_" + withhold, "1")
     phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32", plan=plan)
     st = phobos.phobos_check_device(0)
-    monkeypatch.delenv("PHOBOS_TEST_WITHHOLD_LOAD")
+    monkeypatch.delenv("PHOBOS_TEST_WITHHOLD_" + withhold)
     assert st == phobos.PHOBOS_ERR_TIMEOUT, phobos.status_string(st)
     assert bool((dC == 5.0).all())  # the aborted kernel wrote nothing
     assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK  # the word was cleared

@@ -190,8 +190,9 @@ def test_timing_events_and_launch_count(dev):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()  # torch creates the CUDA events lazily, on first record
     stop.record()
-    # one pre-pass launch (split A and/or B, zero the tail flags), then the main kernel
-    for a_split, launches in ((1, 2), (2, 2)):
+    # one pre-pass launch (split A and/or B, zero the tail flags), then the
+    # main kernel; with the in-kernel panel split the main kernel alone
+    for a_split, launches in ((1, 2), (2, 2), (3, 1)):
         plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
         plan.a_split = a_split
         n0 = phobos.phobos_kernel_launches()
