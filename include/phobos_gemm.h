@@ -118,7 +118,11 @@ typedef enum {
  *                  in a process that is one rank of a multi-process job
  *                  (environment WORLD_SIZE or LOCAL_WORLD_SIZE above 1).
  *  super_m/_n      super-tile: the output tiles are walked super-tile by
- *                  super-tile (an L2-locality group on one GPU).
+ *                  super-tile (an L2-locality group on one GPU).  The planner
+ *                  takes 4096, the pages' smallest super-tile, and super_m =
+ *                  2048 when the kernel splits A and B itself (a_split 3) and
+ *                  M <= 4096, so that the first wave of tiles needs fewer
+ *                  A panels split at once.
  *  super_k         K chunk of the cluster split: super_k < K runs an init
  *                  leaf C = beta*C then one step leaf C += alpha*A_c*B_c per
  *                  chunk (results equal up to rounding order).

@@ -343,7 +343,14 @@ phobos_status_t make_plan(int64_t M, int64_t N, int64_t K, phobos_math_t math,
     p->tile_n = bn;
     p->tile_k = tc_bk(path);
     p->stages = pair ? tc_pair_max_stages(passes, bn) : tc_max_stages(passes, bn);
-    p->super_m = kDefaultSuper;
+    // Raster groups (super-tiles on one GPU) of 4096 rows, the pages' smallest
+    // super-tile.  When the kernel splits A and B itself (split TF32, pairs,
+    // N > 1536) and one such group would cover all of M, the first wave would
+    // need every A panel split at once; groups of 2048 rows cut that demand
+    // (measured on GB300, 4096^3 per call: 0.4431 -> 0.4338 ms; 8192^3 and
+    // 3001 x 5003 x 1999 unchanged within noise).
+    const bool split_inside = pair && passes == 3 && N > kInlineSplitMaxN;
+    p->super_m = split_inside && M <= kDefaultSuper ? kDefaultSuper / 2 : kDefaultSuper;
     p->super_n = kDefaultSuper;
     p->workspace_bytes = tc_workspace(M, N, K, p->tile_m, bn, passes, path);
   }

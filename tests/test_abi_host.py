@@ -106,6 +106,20 @@ def test_plan_paths(lib):
     assert p.path == phobos.PHOBOS_PATH_FFMA
 
 
+def test_plan_raster_groups(lib):
+    # 4096-row raster groups, the pages' smallest super-tile; 2048 rows when
+    # the kernel splits A and B itself (split TF32, CTA pairs, N > 1536) and a
+    # 4096-row group would cover all of M.
+    plan = lambda M, N, K, math="default": phobos.phobos_gemm_plan(M, N, K, K, N, N, math)
+    assert plan(4096, 4096, 4096).super_m == 2048
+    assert plan(3001, 5003, 1999).super_m == 2048
+    assert plan(8192, 8192, 8192).super_m == 4096
+    assert plan(16384, 16384, 16384).super_m == 4096
+    assert plan(4096, 1024, 4096).super_m == 4096        # A split in shared memory
+    assert plan(4096, 4096, 4096, "tf32").super_m == 4096
+    assert plan(65536, 256, 4096).super_m == 4096
+
+
 def test_plan_rejects_unknown_math(lib):
     with pytest.raises(phobos.PhobosError):
         phobos.phobos_gemm_plan(16, 16, 16, 16, 16, 16, 9)
