@@ -227,7 +227,9 @@ phobos_status_t phobos_sgemm_ex(int64_t M, int64_t N, int64_t K, float alpha,
  * buffers owned by the library, runs the GEMM on `stream`, copies C back and
  * synchronizes `stream` before returning.  Problems on the tensor-core path
  * with M >= 2048 run as up to 8 row bands on two internal copy streams so
- * that the copies of later bands overlap the compute of earlier ones.  Same
+ * that the copies of later bands overlap the compute of earlier ones; when
+ * the kernel splits its own operands and K >= 2048, the first band runs in K
+ * chunks that each start as soon as their rows of B have arrived.  Same
  * layout and errors as phobos_sgemm_ex, plus PHOBOS_ERR_OUT_OF_MEMORY for
  * the staging buffers.  Calls are serialised inside the library.
  */

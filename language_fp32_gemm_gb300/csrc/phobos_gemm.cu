@@ -149,9 +149,10 @@ struct Staging {
 std::map<int, Staging> g_staging;
 // Copy streams and events of the host-buffer entry point, per device.
 constexpr int kMaxBands = 8;
+constexpr int kMaxBChunks = 8;  // K chunks of B for the first band (see phobos_sgemm_host)
 struct HostPipe {
   cudaStream_t in = nullptr, out = nullptr;
-  cudaEvent_t ev[2 * kMaxBands + 2] = {};
+  cudaEvent_t ev[2 * kMaxBands + 2 + kMaxBChunks] = {};
   bool ready = false;
 };
 std::map<int, HostPipe> g_pipes;
@@ -485,10 +486,12 @@ phobos_status_t run_ffma(int64_t M, int64_t N, int64_t K, float alpha, const flo
 
 // reuse_b: the previous call on this stream split the same B (same N, K, ldb,
 // mode) into the workspace; skip that pre-pass unless the workspace moved.
+// k_ready (K-chunked plans only): event c is waited for before the step leaf
+// of K chunk c, for callers whose operands arrive chunk by chunk.
 phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                        const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                        cudaStream_t stream, const phobos_gemm_plan_t &p, DeviceState &dev,
-                       int device, bool reuse_b = false) {
+                       int device, bool reuse_b = false, const cudaEvent_t *k_ready = nullptr) {
   const int passes = p.path == PHOBOS_PATH_3XTF32 ? 3 : 1;
   const bool pair = p.cluster_m == 2;
   const bool mc = p.multicast == 1;  // clusters of two pairs sharing A (validated: pairs, tf32)
@@ -712,6 +715,8 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
       t.tail_units = w > 0 ? fill_tail_shares(t, tail, w) : 0;
       if (t.tail_units == 0) t.full_tiles = total_tiles;
     }
+    if (k_ready && cudaStreamWaitEvent(stream, k_ready[t.epoch - 1], 0) != cudaSuccess)
+      return PHOBOS_ERR_CUDA;
     st = cuda_status(counted(pair ? launch_tc_pair(t, passes, bn, p.stages, stream, kind)
                                    : launch_tc(t, passes, bn, p.stages, stream, kind)));
   }
@@ -735,7 +740,8 @@ phobos_status_t read_status_word(DeviceState &dev, cudaStream_t stream) {
 phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                            int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                            int64_t ldc, void *stream_ptr, phobos_math_t math,
-                           const phobos_gemm_plan_t *user_plan, bool reuse_b = false) {
+                           const phobos_gemm_plan_t *user_plan, bool reuse_b = false,
+                           const cudaEvent_t *k_ready = nullptr) {
   phobos_status_t st = check_sizes(M, N, K, lda, ldb, ldc);
   if (st != PHOBOS_OK) return st;
   if (math < PHOBOS_MATH_DEFAULT || math > PHOBOS_MATH_BF16) return PHOBOS_ERR_INVALID_VALUE;
@@ -765,7 +771,7 @@ phobos_status_t sgemm_impl(int64_t M, int64_t N, int64_t K, float alpha, const f
     st = run_ffma(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev);
   } else {
     st = run_tc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, plan, *dev, device,
-                reuse_b);
+                reuse_b, plan.super_k < K ? k_ready : nullptr);
   }
   if (st == PHOBOS_OK && env_flag("PHOBOS_DEBUG_SYNC")) st = read_status_word(*dev, stream);
   return st;
@@ -876,11 +882,28 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, 
   }
   cudaEvent_t ev_start = pipe->ev[0], ev_end = pipe->ev[1];
   cudaEvent_t *ev_in = pipe->ev + 2, *ev_done = pipe->ev + 2 + kMaxBands;
+  cudaEvent_t *ev_b = pipe->ev + 2 + 2 * kMaxBands;
   const int64_t rows = ((M + bands - 1) / bands + 255) / 256 * 256;
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // When the first band's kernel splits its own operands (split TF32 with CTA
+  // pairs and N > 1536), it runs in K chunks: B crosses the link chunk by
+  // chunk right after that band's rows of A and C, and each chunk's step leaf
+  // waits only for its rows of B, so the GEMM starts long before all of B is
+  // in.  The later bands reuse the split of B that those steps leave in the
+  // workspace.  Otherwise all of B goes first.
+  phobos_gemm_plan_t band0_plan;
+  int64_t kc = 0;
+  int n_kc = 0;
+  if (make_plan(rows < M ? rows : M, N, K, math, &band0_plan) == PHOBOS_OK &&
+      band0_plan.path == PHOBOS_PATH_3XTF32 && band0_plan.cluster_m == 2 &&
+      N > kInlineSplitMaxN && K >= 2048) {
+    kc = round_up((K + kMaxBChunks - 1) / kMaxBChunks, 256);
+    n_kc = static_cast<int>((K + kc - 1) / kc);
+    band0_plan.super_k = kc;
+  }
   if (!ok(cudaEventRecord(ev_start, stream)) || !ok(cudaStreamWaitEvent(pipe->in, ev_start, 0)) ||
       !ok(cudaStreamWaitEvent(pipe->out, ev_start, 0)) ||
-      !ok(cudaMemcpyAsync(dB, B, b_elems * 4, cudaMemcpyHostToDevice, pipe->in)))
+      (n_kc == 0 && !ok(cudaMemcpyAsync(dB, B, b_elems * 4, cudaMemcpyHostToDevice, pipe->in))))
     return PHOBOS_ERR_CUDA;
   int used = 0;
   for (int64_t r0 = 0; r0 < M; r0 += rows, ++used) {
@@ -892,6 +915,13 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, 
          !ok(cudaMemcpyAsync(dC + c_off, C + c_off, c_len * 4, cudaMemcpyHostToDevice, pipe->in))) ||
         !ok(cudaEventRecord(ev_in[used], pipe->in)))
       return PHOBOS_ERR_CUDA;
+    for (int c = 0; used == 0 && c < n_kc; ++c) {  // B's K rows, chunk by chunk
+      const int64_t k0 = c * kc, k1 = k0 + kc < K ? k0 + kc : K;
+      const size_t b_off = static_cast<size_t>(k0 * ldb), b_len = static_cast<size_t>((k1 - 1 - k0) * ldb + N);
+      if (!ok(cudaMemcpyAsync(dB + b_off, B + b_off, b_len * 4, cudaMemcpyHostToDevice, pipe->in)) ||
+          !ok(cudaEventRecord(ev_b[c], pipe->in)))
+        return PHOBOS_ERR_CUDA;
+    }
   }
   int band = 0;
   for (int64_t r0 = 0; r0 < M; r0 += rows, ++band) {
@@ -899,8 +929,12 @@ phobos_status_t phobos_sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, 
     const size_t a_off = static_cast<size_t>(r0 * lda);
     const size_t c_off = static_cast<size_t>(r0 * ldc), c_len = static_cast<size_t>((r1 - 1 - r0) * ldc + N);
     if (!ok(cudaStreamWaitEvent(stream, ev_in[band], 0))) return PHOBOS_ERR_CUDA;
-    st = sgemm_impl(r1 - r0, N, K, alpha, dA + a_off, lda, dB, ldb, beta, dC + c_off, ldc,
-                    stream_ptr, math, nullptr, band > 0);
+    if (band == 0 && n_kc > 0)
+      st = sgemm_impl(r1 - r0, N, K, alpha, dA + a_off, lda, dB, ldb, beta, dC + c_off, ldc,
+                      stream_ptr, math, &band0_plan, false, ev_b);
+    else
+      st = sgemm_impl(r1 - r0, N, K, alpha, dA + a_off, lda, dB, ldb, beta, dC + c_off, ldc,
+                      stream_ptr, math, nullptr, band > 0);
     if (st != PHOBOS_OK) return st;
     if (!ok(cudaEventRecord(ev_done[band], stream)) ||
         !ok(cudaStreamWaitEvent(pipe->out, ev_done[band], 0)) ||

@@ -133,6 +133,24 @@ def test_panel_split_host_bands_reuse_the_split_of_b(dev):
     assert oracle.max_rel_error(C, ref, den) <= oracle.TOL_FP32
 
 
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_host_bands_stream_b_in_k_chunks(dev, beta):
+    # With K >= 2048 the first band runs as K-chunked step leaves, each waiting
+    # for its own rows of B on the copy stream: 2048 rows in two bands, K =
+    # 2500 in chunks of 512 (the last one 452 deep), N > 1536.
+    M, N, K = 2048, 1700, 2500
+    A = padded(si.normal(118, 0, (M, K)), 3)
+    B = padded(si.normal(118, 1, (K, N)), 2)
+    C0 = si.uniform_pm1(118, 2, (M, N))
+    C = C0.copy()
+    lda, ldb = A.strides[0] // 4, B.strides[0] // 4
+    st = phobos.phobos_sgemm_host(M, N, K, 1.25, A.ctypes.data, lda, B.ctypes.data, ldb, beta,
+                                  C.ctypes.data, N, 0, phobos.PHOBOS_MATH_DEFAULT)
+    assert st == phobos.PHOBOS_OK
+    ref, den = oracle.sgemm(A, B, C0, 1.25, beta)
+    assert oracle.max_rel_error(C, ref, den) <= oracle.TOL_FP32
+
+
 def test_panel_split_is_the_default_for_wide_split_tf32(dev):
     # The automatic choice (a_split = 0) takes the panel split for N > 1536;
     # the result equals the forced plan's bit for bit.
