@@ -91,6 +91,26 @@ def test_unaligned_pointers(dev, math):
     check(dev, A, B, C0, 1.0, 0.5, math, offsets=(1, 3, 1))
 
 
+@pytest.mark.parametrize("pad", [1, 2, 3])
+@pytest.mark.parametrize("c_offset", [0, 1, 2, 3])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_misaligned_c_rows_bit_exact(dev, pad, c_offset, beta):
+    # ldc = N + pad is not a multiple of 4, so consecutive rows of C start at
+    # different offsets inside their 16-byte chunks (and the offset pointer
+    # shifts them all): the tensor-core epilogue then moves each row through
+    # its own aligned window of 16-byte chunks, with element-wise edges.
+    # Integer inputs make every result exact, so any misplaced, dropped or
+    # duplicated element fails; beta = 0 must not read C (NaN there).
+    M, N, K = 300, 600, 64
+    A = si.integers(40 + pad, 0, (M, K))
+    B = si.integers(40 + pad, 1, (K, N))
+    C0 = si.integers(40 + pad, 2, (M, N)) if beta else np.full((M, N), np.nan, np.float32)
+    C0p = padded(C0, pad)
+    C = run_gemm(torch, dev, A, B, C0p, 1.5, beta, "3xtf32", offsets=(0, 0, c_offset))
+    ref, _ = oracle.sgemm(A, B, C0 if beta else None, 1.5, beta)
+    assert np.array_equal(C, oracle.ref32(ref))
+
+
 @pytest.mark.parametrize("math", MATHS)
 def test_closed_form_zero_b_bit_exact(dev, math):
     M, N, K = 300, 270, 130
