@@ -114,14 +114,27 @@ def normal(seed, stream, shape, sd=1.0):
 
 def integers(seed, stream, shape, lo=-4, hi=4):
     """iid integers uniform on lo..hi, as float32."""
+    shape = tuple(shape)
+    return integer_rows(seed, stream, shape, 0, shape[0], lo, hi)
+
+
+def integer_rows(seed, stream, shape, r0, r1, lo=-4, hi=4):
+    """Rows r0 .. r1-1 of ``integers(seed, stream, shape, lo, hi)``.
+
+    Draw n of the stream is element n of the row-major matrix, so a block of
+    rows is drawn on its own: a matrix larger than host memory can be made and
+    copied block by block.
+    """
     span = hi - lo + 1
-    out = np.empty(int(np.prod(shape)), dtype=np.float32)
+    cols = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    out = np.empty((r1 - r0) * cols, dtype=np.float32)
+    first = r0 * cols
 
     def fn(a, b):
-        x = stream_bits(seed, stream, b - a, a)
+        x = stream_bits(seed, stream, b - a, first + a)
         return ((x >> np.uint64(32)) % np.uint64(span)).astype(np.int64).astype(np.float32) + lo
 
-    return _fill(out, fn).reshape(shape)
+    return _fill(out, fn).reshape((r1 - r0,) + tuple(shape[1:]))
 
 
 def sample_indices(seed, stream, M, N, count, edges=True):

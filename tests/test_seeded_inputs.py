@@ -55,6 +55,19 @@ def test_chunked_generation_matches_unchunked(monkeypatch):
     assert np.array_equal(c, si.normal(9, 1, (3, 1000)))
 
 
+def test_row_blocks_equal_slices_of_the_whole_matrix(monkeypatch):
+    # the large-matrix GPU tests draw and upload a matrix block by block
+    whole = si.integers(21, 3, (37, 53), -2, 2)
+    blocks = [si.integer_rows(21, 3, (37, 53), r0, min(37, r0 + 8), -2, 2) for r0 in range(0, 37, 8)]
+    assert np.array_equal(np.concatenate(blocks), whole)
+    monkeypatch.setattr(si, "_CHUNK", 100)
+    assert np.array_equal(si.integer_rows(21, 3, (37, 53), 30, 37, -2, 2), whole[30:])
+    assert si.integer_rows(21, 3, (37, 53), 5, 5).shape == (0, 53)
+    # element n of the matrix is draw n of the stream
+    x = si.stream_bits(21, 3, 1, 11 * 53 + 7)[0]
+    assert whole[11, 7] == float(int(x >> np.uint64(32)) % 5 - 2)
+
+
 def test_workload_table():
     w = si.workload("sgemm_8192")
     assert (w.M, w.N, w.K, w.alpha, w.beta, w.seed) == (8192, 8192, 8192, 0.75, 0.25, 2)
