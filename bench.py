@@ -34,6 +34,8 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25   # dense tensor rates, nominal
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 SMS, FP32_LANES_PER_SM = 152, 128
+# --split: the plan's a_split values
+SPLITS = {"auto": 0, "prepass": 1, "smem": 2, "kernel": 3}
 
 
 def parse_args():
@@ -49,6 +51,10 @@ def parse_args():
                     help="device-resident steps use the plan's multicast clusters (two CTA "
                          "pairs sharing A); the e2e leg keeps the automatic plan.  One GPU "
                          "only: refused under a multi-rank launch")
+    ap.add_argument("--split", default="auto", choices=sorted(SPLITS),
+                    help="where split TF32 splits A and B (the plan's a_split): the planner's "
+                         "choice, a pre-pass, A in shared memory (B by the pre-pass), or the "
+                         "main kernel's splitter warps.  The e2e leg keeps the automatic plan")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target host time of the oracle baseline sample")
@@ -171,7 +177,7 @@ class ClockSampler:
 
     def start(self):
         cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-               "-lms", "100"]
+               "-lms", "20"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -200,8 +206,12 @@ class ClockSampler:
 
     def summary(self, t_begin, t_end):
         rows = [s for t, s in self.samples if t_begin <= t <= t_end and len(s) >= 8]
-        if not rows:  # a short region: take the samples nearest to it
-            rows = [s for t, s in self.samples if len(s) >= 8][-3:]
+        inside = len(rows)
+        if not rows:  # a region shorter than the sampling interval: the nearest samples
+            mid = 0.5 * (t_begin + t_end)
+            near = sorted((abs(t - mid), i) for i, (t, s) in enumerate(self.samples)
+                          if len(s) >= 8)[:2]
+            rows = [self.samples[i][1] for _, i in sorted(near, key=lambda x: x[1])]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
 
@@ -218,7 +228,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(pw) if pw else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "samples_inside": inside}
 
 
 def oracle_rows_rate(w, A, B, C0, seconds):
@@ -331,6 +341,8 @@ def run_phobos(args):
     plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, args.math)
     if args.multicast:
         plan.multicast, plan.cluster_n = 1, 2
+    plan.a_split = SPLITS[args.split]
+    own_plan = args.multicast or args.split != "auto"
     path_name = {phobos.PHOBOS_PATH_FFMA: "ffma", phobos.PHOBOS_PATH_TF32: "tf32",
                  phobos.PHOBOS_PATH_3XTF32: "3xtf32", phobos.PHOBOS_PATH_FP16: "fp16",
                  phobos.PHOBOS_PATH_BF16: "bf16"}[plan.path]
@@ -338,7 +350,7 @@ def run_phobos(args):
 
     def step():
         phobos.sgemm(dA, dB, dC, w.alpha, w.beta, math=args.math, stream=stream,
-                     plan=plan if args.multicast else None)
+                     plan=plan if own_plan else None)
 
     for _ in range(args.warmup):
         step()
@@ -368,6 +380,7 @@ def run_phobos(args):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = phobos.phobos_kernel_launches()
+    phobos.phobos_kernel_clock_mhz()  # clear the kernels' cycle sum
     wall0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
@@ -381,6 +394,7 @@ def run_phobos(args):
         dist.barrier()
     torch.cuda.synchronize()
     launches = phobos.phobos_kernel_launches() - launches0
+    kernel_mhz = phobos.phobos_kernel_clock_mhz() or None  # tensor-core kernels only
     if clocks:
         clocks.stop()
     st = phobos.phobos_check_device(stream.cuda_stream)
@@ -431,20 +445,28 @@ def run_phobos(args):
     achieved = flops / (avg_kernel_ms / 1e3) / 1e12
     clk = clocks.summary(wall0, wall1) if clocks else None
     # Per-clock view: nominal dense tensor rate per SM (tf32: 4096 flop/clk/SM,
-    # i.e. 1.1 PFLOP/s at ~1.77 GHz; fp16/bf16: 8192) at the SM clock sampled
-    # during the run.
+    # i.e. 1.1 PFLOP/s at ~1.77 GHz; fp16/bf16: 8192) at the SM clock the
+    # kernels counted themselves (cycles over global-timer time), else the one
+    # nvidia-smi sampled.  Under the power cap the clock moves faster than
+    # nvidia-smi samples it.
     per_clock = None
-    if bound == "tensor" and clk and clk.get("sm_mhz"):
-        tf32_clk = SMS * 4096 * clk["sm_mhz"] * 1e6 / 1e12
+    per_clock_mhz = kernel_mhz or (clk.get("sm_mhz") if clk else None)
+    if bound == "tensor" and per_clock_mhz:
+        tf32_clk = SMS * 4096 * per_clock_mhz * 1e6 / 1e12
         per_clock = {"3xtf32": tf32_clk / 3.0, "tf32": tf32_clk}.get(path_name, 2 * tf32_clk)
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": kernel_traffic(kernel_file, args.workload,
-                                                                    path_name, args.multicast),
+                # the committed counters are of the automatic split
+                "frac": achieved / peak,
+                "traffic": kernel_traffic(kernel_file, args.workload, path_name, args.multicast)
+                           if args.split == "auto" else None,
                 "peak_source": "%s (%s)" % (peak_src, peak_note),
                 "kernel": "sgemm_tc_kernel" if path_name != "ffma" else "sgemm_ffma_kernel",
                 "kernel_ms": avg_kernel_ms,
                 "algorithmic_flops_per_launch": flops,
                 "peak_per_clock": per_clock,
+                "kernel_sm_mhz": kernel_mhz,
+                "per_clock_mhz_source": ("kernel cycle counter" if kernel_mhz else
+                                         "nvidia-smi median") if per_clock else None,
                 "frac_per_clock": achieved / per_clock if per_clock else None}
 
     cpu = None
@@ -466,7 +488,7 @@ def run_phobos(args):
         "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "alpha": w.alpha,
                    "beta": w.beta, "seed": w.seed, "math": path_name,
-                   "plan": plan.as_dict(), "parallelism": "replicas" if world > 1 else "single",
+                   "plan": plan.as_dict(), "split": args.split, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (%.0f MiB of A, B, C)"
                          % (4 * (M * K + K * N + M * N) / 2 ** 20),
                    "step": "one library call: split of A and B into tf32 pairs (inside the "

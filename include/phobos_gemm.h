@@ -256,6 +256,20 @@ phobos_status_t phobos_check_device(void *stream);
  */
 phobos_status_t phobos_set_timing_events(void *start, void *stop);
 
+/*
+ * Instrumentation: the SM clock the tensor-core GEMM kernels ran at.  While
+ * timing events are set (phobos_set_timing_events), thread 0 of the first
+ * CTA of every tensor-core GEMM launch on the current device adds the SM
+ * cycles (clock64) and the nanoseconds (%globaltimer) of its CTA's lifetime
+ * to a device-side sum.  This call waits for the current device, stores the
+ * sum's cycles per microsecond in *mhz (0 when no launch was counted since the
+ * last call) and clears the sum.  Under a power cap the SM clock changes
+ * within milliseconds, faster than nvidia-smi samples it; this is the clock of
+ * the kernels themselves.  Returns PHOBOS_ERR_INVALID_VALUE for a NULL mhz,
+ * PHOBOS_ERR_CUDA if a copy fails.
+ */
+phobos_status_t phobos_kernel_clock_mhz(double *mhz);
+
 /* Number of CUDA kernels this library has launched since it was loaded. */
 uint64_t phobos_kernel_launches(void);
 

@@ -47,7 +47,8 @@ MATH_NAMES = {"default": PHOBOS_MATH_DEFAULT, "3xtf32": PHOBOS_MATH_3XTF32,
 
 ABI_FUNCTIONS = ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
                  "phobos_check_device", "phobos_set_timing_events", "phobos_kernel_launches",
-                 "phobos_release", "phobos_status_string", "phobos_sgemm_noalloc")
+                 "phobos_release", "phobos_status_string", "phobos_sgemm_noalloc",
+                 "phobos_kernel_clock_mhz")
 
 # Split operands the no-allocation entry point can hold (bytes).
 PHOBOS_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -102,13 +103,14 @@ def library():
         lib.phobos_check_device.argtypes = [vp]
         lib.phobos_release.argtypes = []
         lib.phobos_set_timing_events.argtypes = [vp, vp]
+        lib.phobos_kernel_clock_mhz.argtypes = [ctypes.POINTER(ctypes.c_double)]
         lib.phobos_kernel_launches.argtypes = []
         lib.phobos_kernel_launches.restype = ctypes.c_uint64
         lib.phobos_status_string.argtypes = [i32]
         lib.phobos_status_string.restype = ctypes.c_char_p
         for name in ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
                      "phobos_check_device", "phobos_release", "phobos_set_timing_events",
-                     "phobos_sgemm_noalloc"):
+                     "phobos_sgemm_noalloc", "phobos_kernel_clock_mhz"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -171,6 +173,16 @@ def phobos_set_timing_events(start, stop):
 
 def phobos_kernel_launches():
     return library().phobos_kernel_launches()
+
+
+def phobos_kernel_clock_mhz():
+    """Average SM clock (MHz) of the tensor-core kernels launched while timing
+    events were set, since the last call (0.0 if none); clears the sum."""
+    mhz = ctypes.c_double(0.0)
+    st = library().phobos_kernel_clock_mhz(ctypes.byref(mhz))
+    if st != PHOBOS_OK:
+        raise PhobosError(st, "phobos_kernel_clock_mhz")
+    return mhz.value
 
 
 # ----------------------------------------------------------- torch tensors

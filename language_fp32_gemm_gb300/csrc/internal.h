@@ -134,6 +134,10 @@ struct TcArgs {
   int vec_a, vec_b;  // 16-byte loads of the raw operands allowed
   unsigned *split_flags;
   unsigned *split_next;
+  // Instrumentation (nullptr = off): thread 0 of CTA 0 adds the SM cycles
+  // (clock64) and the nanoseconds (%globaltimer) of its CTA's lifetime to
+  // clock_acc[0] and clock_acc[1], which gives the SM clock the kernel ran at.
+  unsigned long long *clock_acc;
 };
 // K blocks per item of the in-kernel panel split (256 of K).  Measured on
 // GB300: items of 64 of K spent more time in their flag fences and round trips

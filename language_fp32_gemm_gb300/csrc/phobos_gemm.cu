@@ -130,6 +130,9 @@ struct DeviceState {
   bool supported = false;
   int sm_count = 0;
   int *err = nullptr;  // device status word
+  // SM cycles and nanoseconds summed by the tensor-core kernels while timing
+  // events are set (allocated on first use)
+  unsigned long long *clock_acc = nullptr;
   // resident clusters of the multicast pair kernel, one pass / three passes
   // (0 = not queried yet)
   int mc_clusters[2] = {0, 0};
@@ -683,6 +686,15 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   t.flags = flags;
   t.epoch = 1;
   t.err = dev.err;
+  if (g_ev_start) {  // instrumentation on: the kernels also sum their SM cycles
+    if (!dev.clock_acc) {
+      if (cudaMalloc(&dev.clock_acc, 2 * sizeof(unsigned long long)) != cudaSuccess)
+        return PHOBOS_ERR_OUT_OF_MEMORY;
+      if (cudaMemset(dev.clock_acc, 0, 2 * sizeof(unsigned long long)) != cudaSuccess)
+        return PHOBOS_ERR_CUDA;
+    }
+    t.clock_acc = dev.clock_acc;
+  }
   const int total_blocks = static_cast<int>(Kp / bk);
   if (p.super_k >= K) {
     t.alpha = alpha;
@@ -972,6 +984,23 @@ phobos_status_t phobos_set_timing_events(void *start, void *stop) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_ev_start = static_cast<cudaEvent_t>(start);
   g_ev_stop = static_cast<cudaEvent_t>(stop);
+  return PHOBOS_OK;
+}
+
+phobos_status_t phobos_kernel_clock_mhz(double *mhz) {
+  if (!mhz) return PHOBOS_ERR_INVALID_VALUE;
+  *mhz = 0.0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState *dev = nullptr;
+  phobos_status_t st = device_state(&dev, nullptr);
+  if (st != PHOBOS_OK) return st;
+  if (!dev->clock_acc) return PHOBOS_OK;
+  unsigned long long acc[2] = {0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(acc, dev->clock_acc, sizeof(acc), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(dev->clock_acc, 0, sizeof(acc)) != cudaSuccess)
+    return PHOBOS_ERR_CUDA;
+  if (acc[1] > 0) *mhz = 1e3 * static_cast<double>(acc[0]) / static_cast<double>(acc[1]);
   return PHOBOS_OK;
 }
 

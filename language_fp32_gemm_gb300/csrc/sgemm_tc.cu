@@ -499,6 +499,15 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   const uint32_t a_full0 = mma_drained + 8u;     // this CTA's raw A tile landed
   const uint32_t conv0 = a_full0 + 8u * STAGES;  // A tile split (leader: both CTAs)
 
+  // (instrumentation) the SM clock over this CTA's lifetime, in CTA 0 only
+  const bool clock_probe = p.clock_acc != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+  long long probe_cycles = 0;
+  unsigned long long probe_ns = 0;
+  if (clock_probe) {
+    probe_ns = global_ns();
+    probe_cycles = clock64();
+  }
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Cluster layout: one CTA, one CTA pair (ranks 0, 1), or with multicast two
@@ -1182,6 +1191,12 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       tmem_dealloc_pair(tmem_base, S::kTmemCols);
     else
       tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+  if (clock_probe) {  // every warp of the CTA has passed the barrier above
+    const long long cycles = clock64() - probe_cycles;
+    const unsigned long long ns = global_ns() - probe_ns;
+    atomicAdd(p.clock_acc, static_cast<unsigned long long>(cycles));
+    atomicAdd(p.clock_acc + 1, ns);
   }
 }
 

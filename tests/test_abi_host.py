@@ -120,6 +120,11 @@ def test_plan_raster_groups(lib):
     assert plan(65536, 256, 4096).super_m == 4096
 
 
+def test_kernel_clock_reader_rejects_null(lib):
+    # argument check before any device call
+    assert lib.phobos_kernel_clock_mhz(None) == phobos.PHOBOS_ERR_INVALID_VALUE
+
+
 def test_plan_rejects_unknown_math(lib):
     with pytest.raises(phobos.PhobosError):
         phobos.phobos_gemm_plan(16, 16, 16, 16, 16, 16, 9)

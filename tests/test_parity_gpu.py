@@ -384,3 +384,27 @@ def test_same_sign_inputs_within_their_accumulation_bound(dev, math, K):
         U = 3 * 4 * promote_blocks(K)
         bound = U * 2.0 ** -23 / 4 + 2.0 ** -21
     assert err <= bound, "max rel error %.3g > %.3g" % (err, bound)
+
+
+def test_kernels_count_their_sm_clock_only_while_timed(dev):
+    # phobos_kernel_clock_mhz: the tensor-core kernels add their SM cycles and
+    # global-timer nanoseconds to a device sum while timing events are set.
+    M = N = K = 2048
+    dA = torch.from_numpy(si.normal(97, 0, (M, K))).to(dev)
+    dB = torch.from_numpy(si.normal(97, 1, (K, N))).to(dev)
+    dC = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    phobos.phobos_kernel_clock_mhz()  # clear
+    phobos.sgemm(dA, dB, dC, 1.0, 0.0)
+    assert phobos.phobos_kernel_clock_mhz() == 0.0  # not timed: nothing counted
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    phobos.phobos_set_timing_events(start.cuda_event, stop.cuda_event)
+    try:
+        for _ in range(3):
+            phobos.sgemm(dA, dB, dC, 1.0, 0.0)
+    finally:
+        phobos.phobos_set_timing_events(None, None)
+    mhz = phobos.phobos_kernel_clock_mhz()
+    assert 300.0 < mhz < 2500.0, mhz
+    assert phobos.phobos_kernel_clock_mhz() == 0.0  # the read cleared the sum
+    assert start.elapsed_time(stop) > 0.0
+    assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK
