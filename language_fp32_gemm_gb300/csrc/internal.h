@@ -134,6 +134,9 @@ struct TcArgs {
   int vec_a, vec_b;  // 16-byte loads of the raw operands allowed
   unsigned *split_flags;
   unsigned *split_next;
+  // split_done[epoch - 1] counts the launch's published items; once it equals
+  // their number, a producer stops waiting on flags for the rest of the launch
+  unsigned *split_done;
   // Instrumentation (nullptr = off): thread 0 of CTA 0 adds the SM cycles
   // (clock64) and the nanoseconds (%globaltimer) of its CTA's lifetime to
   // clock_acc[0] and clock_acc[1], which gives the SM clock the kernel ran at.

@@ -551,12 +551,12 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int64_t slots = static_cast<int64_t>(tail_units) * (mc ? 2 : 1);  // one partial sum per pair at most
   const size_t part_bytes = static_cast<size_t>(round_up(slots * bm * bn * 4, 256));
   // flags: the tail split's, then (in-kernel panel split) one per item of the
-  // longest launch and one item counter per launch
+  // longest launch and two item counters per launch (claimed, done)
   const int64_t tail_flags = slots * 2 * kEpiWarps;
   const int64_t chunk_kc = (chunk_blocks_max + kSplitChunkBlocks - 1) / kSplitChunkBlocks;
   const int64_t launches = p.super_k < K ? (Kp / bk + chunk_blocks_max - 1) / chunk_blocks_max : 1;
   const int64_t split_flags = split_inline ? (Mp / bm + Np / bn) * chunk_kc * 8 : 0;
-  const int64_t split_counters = split_inline ? launches : 0;
+  const int64_t split_counters = split_inline ? 2 * launches : 0;  // claimed, done
   const size_t flag_bytes =
       static_cast<size_t>(round_up((tail_flags + split_flags + split_counters) * 4, 256));
   const size_t need = ops_bytes + part_bytes + flag_bytes;
@@ -656,6 +656,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
     t.vec_b = (ldb % 4 == 0) && aligned16(B) ? 1 : 0;
     t.split_flags = flags + tail_flags;
     t.split_next = flags + tail_flags + split_flags;
+    t.split_done = t.split_next + launches;
   }
   t.C = C;
   t.ldc = ldc;

@@ -445,6 +445,12 @@ __device__ __forceinline__ void st_release_gpu(unsigned *addr, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
+// Add v at GPU scope with release semantics: this thread's earlier writes
+// (and those its fences cover) are visible to whoever acquires the sum.
+__device__ __forceinline__ void red_release_gpu_add(unsigned *addr, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *addr) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
@@ -468,13 +474,6 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 // loads of data written by ordinary stores.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Nanoseconds of the GPU's global timer (the same on every SM).
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 // ------------------------------------------------------------------- convert

@@ -406,6 +406,7 @@ __device__ __forceinline__ void split_item(const TcArgs &p, const SplitOrder &or
     const long long f =
         (static_cast<long long>(is_b ? ord.tiles_m + panel : panel) * ord.kc_n + kc) * 8 + slice;
     st_release_gpu(p.split_flags + f, p.epoch);
+    red_release_gpu_add(p.split_done + (p.epoch - 1), 1u);
   }
 }
 
@@ -434,13 +435,19 @@ __device__ void run_splitter(const TcArgs &p, int units, int lane, volatile int 
 // CTA loads for K chunk kc of tile (tm, tn) are split.  Bounded like every
 // wait of the kernel.
 __device__ __forceinline__ bool wait_split_chunk(const TcArgs &p, int tm, int tn, int kc,
-                                                 uint32_t rank, volatile int *abort_flag) {
+                                                 uint32_t rank, volatile int *abort_flag,
+                                                 bool &all_split) {
   const int kc_n = (p.k_blocks + kSplitChunkBlocks - 1) / kSplitChunkBlocks;
+  // every item of this launch (far below 2^32 for any problem that fits the
+  // device: each is 32 x 256 elements of A or B)
+  const unsigned items =
+      static_cast<unsigned>(kc_n) * 8u * static_cast<unsigned>(p.tiles_m + (p.split_b ? p.tiles_n : 0));
   const unsigned *fa = p.split_flags + (static_cast<long long>(tm) * kc_n + kc) * 8 + 4 * rank;
   const unsigned *fb =
       p.split_flags + (static_cast<long long>(p.tiles_m + tn) * kc_n + kc) * 8 + 4 * rank;
   const unsigned e = p.epoch;
   auto ready = [&]() {
+    const unsigned done = ld_relaxed_gpu(p.split_done + (e - 1));
     const unsigned a0 = ld_relaxed_gpu(fa), a1 = ld_relaxed_gpu(fa + 1);
     const unsigned a2 = ld_relaxed_gpu(fa + 2), a3 = ld_relaxed_gpu(fa + 3);
     bool ok = a0 == e && a1 == e && a2 == e && a3 == e;
@@ -449,7 +456,8 @@ __device__ __forceinline__ bool wait_split_chunk(const TcArgs &p, int tm, int tn
       const unsigned b2 = ld_relaxed_gpu(fb + 2), b3 = ld_relaxed_gpu(fb + 3);
       ok = ok && b0 == e && b1 == e && b2 == e && b3 == e;
     }
-    return ok;
+    if (done == items) all_split = true;  // no later chunk needs a wait
+    return ok || all_split;
   };
   if (!ready()) {
     const uint64_t t0 = globaltimer_ns();
@@ -462,8 +470,8 @@ __device__ __forceinline__ bool wait_split_chunk(const TcArgs &p, int tm, int tn
       }
     }
   }
-  fence_acq_rel_gpu();         // the flags' acquire: the split stores happen-before
-  fence_proxy_async_global();  // ... the TMA loads issued after this
+  fence_acq_rel_gpu();         // the flags' (or the count's) acquire: the split
+  fence_proxy_async_global();  // stores happen-before the TMA loads issued after this
   return true;
 }
 
@@ -502,9 +510,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   // (instrumentation) the SM clock over this CTA's lifetime, in CTA 0 only
   const bool clock_probe = p.clock_acc != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
   long long probe_cycles = 0;
-  unsigned long long probe_ns = 0;
+  uint64_t probe_ns = 0;
   if (clock_probe) {
-    probe_ns = global_ns();
+    probe_ns = globaltimer_ns();
     probe_cycles = clock64();
   }
 
@@ -723,6 +731,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       uint32_t armed = 0, last_parity = 0;
       int g = 0;  // k blocks loaded so far by this CTA: ring slot and phase
       bool ok = true;
+      bool all_split = false;  // in-kernel split: every item of the launch is done
       Unit u;
       for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
         int tm, tn;
@@ -734,8 +743,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
           const uint32_t ph = (g / STAGES) & 1u;
           // In-kernel panel split: this CTA's rows of A and B for the K chunk
           // starting here must have been split into the workspace.
-          if (INL && (kb == u.k_lo || kb % kSplitChunkBlocks == 0) &&
-              !wait_split_chunk(p, tm, tn, kb / kSplitChunkBlocks, rank, abort_flag)) {
+          if (INL && !all_split && (kb == u.k_lo || kb % kSplitChunkBlocks == 0) &&
+              !wait_split_chunk(p, tm, tn, kb / kSplitChunkBlocks, rank, abort_flag,
+                                all_split)) {
             abort_peer();
             ok = false;
             break;
@@ -1194,9 +1204,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   }
   if (clock_probe) {  // every warp of the CTA has passed the barrier above
     const long long cycles = clock64() - probe_cycles;
-    const unsigned long long ns = global_ns() - probe_ns;
+    const uint64_t ns = globaltimer_ns() - probe_ns;
     atomicAdd(p.clock_acc, static_cast<unsigned long long>(cycles));
-    atomicAdd(p.clock_acc + 1, ns);
+    atomicAdd(p.clock_acc + 1, static_cast<unsigned long long>(ns));
   }
 }
 

@@ -397,6 +397,10 @@ def test_kernels_count_their_sm_clock_only_while_timed(dev):
     phobos.sgemm(dA, dB, dC, 1.0, 0.0)
     assert phobos.phobos_kernel_clock_mhz() == 0.0  # not timed: nothing counted
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()  # torch creates the CUDA events on their first record
+    stop.record()
+    torch.cuda.synchronize()
+    assert start.cuda_event and stop.cuda_event
     phobos.phobos_set_timing_events(start.cuda_event, stop.cuda_event)
     try:
         for _ in range(3):
