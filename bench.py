@@ -55,6 +55,10 @@ def parse_args():
                     help="where split TF32 splits A and B (the plan's a_split): the planner's "
                          "choice, a pre-pass, A in shared memory (B by the pre-pass), or the "
                          "main kernel's splitter warps.  The e2e leg keeps the automatic plan")
+    ap.add_argument("--clc", action="store_true",
+                    help="device-resident steps deal tiles to CTA pairs through Cluster Launch "
+                         "Control (plan clc = 1, split TF32 only) instead of the static "
+                         "persistent walk; the e2e leg keeps the automatic plan")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target host time of the oracle baseline sample")
@@ -342,7 +346,8 @@ def run_phobos(args):
     if args.multicast:
         plan.multicast, plan.cluster_n = 1, 2
     plan.a_split = SPLITS[args.split]
-    own_plan = args.multicast or args.split != "auto"
+    plan.clc = 1 if args.clc else 0
+    own_plan = args.multicast or args.split != "auto" or args.clc
     path_name = {phobos.PHOBOS_PATH_FFMA: "ffma", phobos.PHOBOS_PATH_TF32: "tf32",
                  phobos.PHOBOS_PATH_3XTF32: "3xtf32", phobos.PHOBOS_PATH_FP16: "fp16",
                  phobos.PHOBOS_PATH_BF16: "bf16"}[plan.path]
@@ -458,7 +463,7 @@ def run_phobos(args):
                 # the committed counters are of the automatic split
                 "frac": achieved / peak,
                 "traffic": kernel_traffic(kernel_file, args.workload, path_name, args.multicast)
-                           if args.split == "auto" else None,
+                           if args.split == "auto" and not args.clc else None,
                 "peak_source": "%s (%s)" % (peak_src, peak_note),
                 "kernel": "sgemm_tc_kernel" if path_name != "ffma" else "sgemm_ffma_kernel",
                 "kernel_ms": avg_kernel_ms,
@@ -488,7 +493,8 @@ def run_phobos(args):
         "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "alpha": w.alpha,
                    "beta": w.beta, "seed": w.seed, "math": path_name,
-                   "plan": plan.as_dict(), "split": args.split, "parallelism": "replicas" if world > 1 else "single",
+                   "plan": plan.as_dict(), "split": args.split, "clc": bool(args.clc),
+                   "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (%.0f MiB of A, B, C)"
                          % (4 * (M * K + K * N + M * N) / 2 ** 20),
                    "step": "one library call: split of A and B into tf32 pairs (inside the "

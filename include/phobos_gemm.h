@@ -164,6 +164,20 @@ typedef enum {
  *                       leading dimension and alignment.
  *                  Identical results whichever is used.  FP16 and BF16 always
  *                  convert A in the pre-pass (0 or 1).
+ *  clc             split-TF32 CTA pairs without multicast or a_split = 2:
+ *                  1 = Cluster Launch Control deals the tiles ("Clusters et
+ *                  DSMEM", 3.7, Cluster Launch Control).  The grid holds one
+ *                  CTA pair per output tile; each resident pair starts on its
+ *                  own tile and then takes tiles from the hardware's queue of
+ *                  pairs not yet launched (it cancels their launch), so pairs
+ *                  that finish early, or start late because other work holds
+ *                  SMs, take more tiles.  The tail split is off (tail_split
+ *                  is ignored); with a_split = 0 the kernel splits A and B
+ *                  itself.  Each tile's result equals the static walk's with
+ *                  tail_split = 1, bit for bit.  0 (the planner's choice) =
+ *                  a static persistent walk: one pair per SM pair, tiles
+ *                  strided over the pairs.  Other plans with clc = 1 give
+ *                  PHOBOS_ERR_UNSUPPORTED.
  *  FP16 and BF16 plans run the tensor-core kernel with its deepest stage ring
  *  only (stages must equal the planner's value).
  */
@@ -177,6 +191,7 @@ typedef struct {
   size_t workspace_bytes;
   int32_t tail_split;
   int32_t a_split;
+  int32_t clc;
 } phobos_gemm_plan_t;
 
 /*
@@ -269,6 +284,16 @@ phobos_status_t phobos_set_timing_events(void *start, void *stop);
  * PHOBOS_ERR_CUDA if a copy fails.
  */
 phobos_status_t phobos_kernel_clock_mhz(double *mhz);
+
+/*
+ * Instrumentation: the output tiles that Cluster Launch Control launches
+ * (plan clc = 1) on the current device took from cancelled pair launches
+ * while timing events were set, since the last call.  Waits for the device,
+ * stores the count in *tiles and clears it.  A grid of T tiles of which P
+ * pairs start at once hands out T - P tiles this way.  Returns
+ * PHOBOS_ERR_INVALID_VALUE for a NULL tiles, PHOBOS_ERR_CUDA if a copy fails.
+ */
+phobos_status_t phobos_kernel_clc_tiles(uint64_t *tiles);
 
 /* Number of CUDA kernels this library has launched since it was loaded. */
 uint64_t phobos_kernel_launches(void);

@@ -48,7 +48,7 @@ MATH_NAMES = {"default": PHOBOS_MATH_DEFAULT, "3xtf32": PHOBOS_MATH_3XTF32,
 ABI_FUNCTIONS = ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
                  "phobos_check_device", "phobos_set_timing_events", "phobos_kernel_launches",
                  "phobos_release", "phobos_status_string", "phobos_sgemm_noalloc",
-                 "phobos_kernel_clock_mhz")
+                 "phobos_kernel_clock_mhz", "phobos_kernel_clc_tiles")
 
 # Split operands the no-allocation entry point can hold (bytes).
 PHOBOS_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -62,7 +62,8 @@ class PhobosGemmPlan(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("multicast", ctypes.c_int32),
                 ("super_m", ctypes.c_int64), ("super_n", ctypes.c_int64),
                 ("super_k", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t),
-                ("tail_split", ctypes.c_int32), ("a_split", ctypes.c_int32)]
+                ("tail_split", ctypes.c_int32), ("a_split", ctypes.c_int32),
+                ("clc", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -104,13 +105,15 @@ def library():
         lib.phobos_release.argtypes = []
         lib.phobos_set_timing_events.argtypes = [vp, vp]
         lib.phobos_kernel_clock_mhz.argtypes = [ctypes.POINTER(ctypes.c_double)]
+        lib.phobos_kernel_clc_tiles.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
         lib.phobos_kernel_launches.argtypes = []
         lib.phobos_kernel_launches.restype = ctypes.c_uint64
         lib.phobos_status_string.argtypes = [i32]
         lib.phobos_status_string.restype = ctypes.c_char_p
         for name in ("phobos_gemm_plan", "phobos_sgemm", "phobos_sgemm_ex", "phobos_sgemm_host",
                      "phobos_check_device", "phobos_release", "phobos_set_timing_events",
-                     "phobos_sgemm_noalloc", "phobos_kernel_clock_mhz"):
+                     "phobos_sgemm_noalloc", "phobos_kernel_clock_mhz",
+                     "phobos_kernel_clc_tiles"):
             getattr(lib, name).restype = i32
         _lib = lib
     return _lib
@@ -173,6 +176,16 @@ def phobos_set_timing_events(start, stop):
 
 def phobos_kernel_launches():
     return library().phobos_kernel_launches()
+
+
+def phobos_kernel_clc_tiles():
+    """Tiles that Cluster Launch Control launches took from cancelled pair
+    launches while timing events were set, since the last call; clears it."""
+    n = ctypes.c_uint64(0)
+    st = library().phobos_kernel_clc_tiles(ctypes.byref(n))
+    if st != PHOBOS_OK:
+        raise PhobosError(st, "phobos_kernel_clc_tiles")
+    return n.value
 
 
 def phobos_kernel_clock_mhz():

@@ -137,9 +137,19 @@ struct TcArgs {
   // split_done[epoch - 1] counts the launch's published items; once it equals
   // their number, a producer stops waiting on flags for the rest of the launch
   unsigned *split_done;
+  // Cluster Launch Control (CTA pairs of split TF32 without the shared-memory A
+  // split or multicast).  1: the grid holds one pair per output tile; a
+  // resident pair starts on its own tile and takes every further tile from
+  // the hardware by cancelling the launch of a pair that has not started, so
+  // tiles are dealt to pairs as they free up.  No tail split.  clc_units:
+  // the pairs that fit on the device at once (the in-kernel split orders its
+  // items by their waves).
+  int clc, clc_units;
   // Instrumentation (nullptr = off): thread 0 of CTA 0 adds the SM cycles
   // (clock64) and the nanoseconds (%globaltimer) of its CTA's lifetime to
-  // clock_acc[0] and clock_acc[1], which gives the SM clock the kernel ran at.
+  // clock_acc[0] and clock_acc[1], which gives the SM clock the kernel ran at;
+  // with Cluster Launch Control every tile taken from a cancelled launch adds
+  // one to clock_acc[2].
   unsigned long long *clock_acc;
 };
 // K blocks per item of the in-kernel panel split (256 of K).  Measured on

@@ -130,8 +130,8 @@ struct DeviceState {
   bool supported = false;
   int sm_count = 0;
   int *err = nullptr;  // device status word
-  // SM cycles and nanoseconds summed by the tensor-core kernels while timing
-  // events are set (allocated on first use)
+  // SM cycles, nanoseconds and tiles taken from cancelled launches, summed by
+  // the tensor-core kernels while timing events are set (allocated on first use)
   unsigned long long *clock_acc = nullptr;
   // resident clusters of the multicast pair kernel, one pass / three passes
   // (0 = not queried yet)
@@ -393,6 +393,13 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (p.super_k <= 0 || p.super_m <= 0 || p.super_n <= 0) return PHOBOS_ERR_INVALID_VALUE;
   if (p.tail_split < 0 || p.tail_split > kMaxTailSplit) return PHOBOS_ERR_INVALID_VALUE;
   if (p.a_split < 0 || p.a_split > 3) return PHOBOS_ERR_INVALID_VALUE;
+  if (p.clc != 0 && p.clc != 1) return PHOBOS_ERR_INVALID_VALUE;
+  // Cluster Launch Control deals tiles to split-TF32 CTA pairs that read A
+  // from the workspace (the kernel's barrier block has room for its state at
+  // that ring depth)
+  if (p.clc == 1 &&
+      (p.cluster_m != 2 || mc || p.path != PHOBOS_PATH_3XTF32 || p.a_split == 2 || p.stages > 4))
+    return PHOBOS_ERR_UNSUPPORTED;
   // the in-kernel panel split runs in tf32 CTA pairs without multicast
   if (p.a_split == 3 && (p.cluster_m != 2 || mc ||
                          (p.path != PHOBOS_PATH_TF32 && p.path != PHOBOS_PATH_3XTF32)))
@@ -518,7 +525,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   } else if (p.a_split == 3) {
     split_inline = true;  // validated: tf32 CTA pairs, no multicast, deepest ring
   } else if (p.a_split == 0 && !mc && p.stages == max_st) {
-    a_inline = a_tma_ok && N <= kInlineSplitMaxN;
+    a_inline = !p.clc && a_tma_ok && N <= kInlineSplitMaxN;
     split_inline = !a_inline && pair && passes == 3;
   }
   const int64_t a_bytes = round_up(Mp * Kp * elem, 256), b_bytes = round_up(Np * Kp * elem, 256);
@@ -545,7 +552,8 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int total_tiles = static_cast<int>((Mp / bm) * walk_n);
   const int chunk_blocks_max =
       static_cast<int>(round_up(p.super_k < K ? p.super_k : K, bk) / bk);
-  const int tail = units > 0 ? total_tiles % units : 0;
+  // (Cluster Launch Control: whole tiles only, dealt by the hardware)
+  const int tail = units > 0 && !p.clc ? total_tiles % units : 0;
   const int tail_units = tail_workers(p.tail_split, tail, units, chunk_blocks_max);
   const int full_tiles = tail_units > 0 ? total_tiles - tail : total_tiles;
   const int64_t slots = static_cast<int64_t>(tail_units) * (mc ? 2 : 1);  // one partial sum per pair at most
@@ -683,15 +691,20 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   // workers sharing the tail are launched
   t.grid_units = tail_units > 0 ? (full_tiles > 0 ? units : tail_units)
                                 : (total_tiles < units ? total_tiles : units);
+  if (p.clc) {  // a pair per tile; the resident ones take the rest
+    t.clc = 1;
+    t.clc_units = units;
+    t.grid_units = total_tiles;
+  }
   t.partials = partials;
   t.flags = flags;
   t.epoch = 1;
   t.err = dev.err;
   if (g_ev_start) {  // instrumentation on: the kernels also sum their SM cycles
     if (!dev.clock_acc) {
-      if (cudaMalloc(&dev.clock_acc, 2 * sizeof(unsigned long long)) != cudaSuccess)
+      if (cudaMalloc(&dev.clock_acc, 3 * sizeof(unsigned long long)) != cudaSuccess)
         return PHOBOS_ERR_OUT_OF_MEMORY;
-      if (cudaMemset(dev.clock_acc, 0, 2 * sizeof(unsigned long long)) != cudaSuccess)
+      if (cudaMemset(dev.clock_acc, 0, 3 * sizeof(unsigned long long)) != cudaSuccess)
         return PHOBOS_ERR_CUDA;
     }
     t.clock_acc = dev.clock_acc;
@@ -1002,6 +1015,23 @@ phobos_status_t phobos_kernel_clock_mhz(double *mhz) {
       cudaMemset(dev->clock_acc, 0, sizeof(acc)) != cudaSuccess)
     return PHOBOS_ERR_CUDA;
   if (acc[1] > 0) *mhz = 1e3 * static_cast<double>(acc[0]) / static_cast<double>(acc[1]);
+  return PHOBOS_OK;
+}
+
+phobos_status_t phobos_kernel_clc_tiles(uint64_t *tiles) {
+  if (!tiles) return PHOBOS_ERR_INVALID_VALUE;
+  *tiles = 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState *dev = nullptr;
+  phobos_status_t st = device_state(&dev, nullptr);
+  if (st != PHOBOS_OK) return st;
+  if (!dev->clock_acc) return PHOBOS_OK;
+  unsigned long long n = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&n, dev->clock_acc + 2, sizeof(n), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(dev->clock_acc + 2, 0, sizeof(n)) != cudaSuccess)
+    return PHOBOS_ERR_CUDA;
+  *tiles = n;
   return PHOBOS_OK;
 }
 

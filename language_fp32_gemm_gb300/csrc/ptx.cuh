@@ -17,6 +17,7 @@ enum : int {
   kDevTimeoutDrain = 0x104,
   kDevTimeoutPartial = 0x105,
   kDevTimeoutSplit = 0x106,  // a producer's wait for split operand panels
+  kDevTimeoutClc = 0x107,    // a wait in the Cluster Launch Control tile walk
 };
 
 // A wait gives up after this much wall time (nanoseconds, %globaltimer).
@@ -108,6 +109,46 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
 
 // Bring one box of a tensor map into L2 (no shared memory, no barrier); the
 // x coordinate follows the same 16-byte rule as a load.
+// ---------------------------------------------------- cluster launch control
+
+// Ask the hardware to cancel the launch of a cluster that has not started
+// yet; the 16-byte answer lands at `resp` (shared, 16-byte aligned) and
+// completes 16 bytes of transactions on mbarrier `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// The x index of the first CTA of the cluster an answer cancelled, or -1
+// when the request cancelled nothing (no cluster was left to launch).
+__device__ __forceinline__ int clc_cancelled_ctaid_x(uint32_t resp) {
+  int x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "mov.s32 %0, -1;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t"
+      "}"
+      : "=r"(x)
+      : "r"(resp)
+      : "memory");
+  return x;
+}
+
+__device__ __forceinline__ void st_shared_s32(uint32_t addr, int v) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),

@@ -497,6 +497,15 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   // then (in-kernel A split) [2S+5, 3S+5) a_full, [3S+5, 4S+5) converted
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * STAGES + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  // Cluster Launch Control state after the abort flag (16-byte aligned): the
+  // hardware's answer and its barrier, then a two-entry ring of tile indices
+  // with full barriers (both CTAs) and empty barriers (the leader's).
+  constexpr bool kClcKernel = PAIR && !ASPLIT && !MC && (4 * STAGES + 5) * 8 + 8 + 64 <= 256;
+  const uint32_t clc_resp = smem_u32(tmem_slot + 2);
+  const uint32_t clc_full = clc_resp + 16u;
+  const uint32_t tile_full0 = clc_resp + 24u;
+  const uint32_t tile_empty0 = clc_resp + 40u;
+  const uint32_t tile_ring0 = clc_resp + 56u;
   float *epi_stage = reinterpret_cast<float *>(aux + 256);  // kEpiWarps x 32 x 32 floats
 
   const uint32_t full0 = smem_u32(bars);
@@ -557,6 +566,84 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   };
   const int chunk = p.promote_blocks;
 
+  // ------------------------------------------------------------ tile walk
+  // Static: unit_of's stride over the persistent grid.  With Cluster Launch
+  // Control the grid holds a pair per tile; a resident pair starts on its own
+  // tile and its leader's producer gets every further tile from the hardware:
+  // it asks (try_cancel) while it loads the current tile, then publishes the
+  // answer as entry e of a two-entry ring in both CTAs.  The MMA issuer, the
+  // peer's producer and every thread of the accumulator warps read the ring
+  // and release the entry on the leader, one arrival each.  Entry -1 ends the
+  // walk.
+  const bool clc = kClcKernel && p.clc != 0;
+  constexpr int kClcReaders = 2 * (1 + 32 * kEpiWarps);
+  // the units the in-kernel split's item order expects to run at once
+  const int walk_units = clc ? p.clc_units : units;
+  bool clc_pending = false;  // (leader's producer) a request is in flight
+  uint32_t clc_phase = 0;
+  auto clc_request = [&]() {
+    mbar_arrive_expect_tx(clc_full, 16u);
+    clc_try_cancel(clc_resp, clc_full);
+    clc_pending = true;
+  };
+  // (leader's producer) entry e >= 1: the next tile, -1 at the end, -2 when a
+  // wait ran out
+  auto clc_publish = [&](int e) -> int {
+    int t = -1;
+    if (clc_pending) {
+      if (!bounded_wait(clc_full, clc_phase, abort_flag, p.err, kDevTimeoutClc)) return -2;
+      clc_phase ^= 1u;
+      clc_pending = false;
+      const int x = clc_cancelled_ctaid_x(clc_resp);
+      if (x >= 0) {
+        t = x / 2;  // the first CTA of a pair has an even index
+        if (t >= p.tiles_m * p.tiles_n) {  // not a tile of this grid: stop, and say so
+          *abort_flag = 1;
+          atomicCAS(p.err, 0, kDevTimeoutClc);
+          return -2;
+        }
+        if (p.clock_acc) atomicAdd(p.clock_acc + 2, 1ull);  // (instrumentation)
+        clc_request();
+      }
+    }
+    const uint32_t s = static_cast<uint32_t>(e - 1) & 1u;
+    const uint32_t ph = (static_cast<uint32_t>(e - 1) >> 1) & 1u;
+    if (!bounded_wait_cluster(tile_empty0 + 8u * s, ph ^ 1u, abort_flag, p.err, kDevTimeoutClc))
+      return -2;
+    st_shared_s32(tile_ring0 + 4u * s, t);
+    st_shared_cluster_u32(mapa_shared(tile_ring0 + 4u * s, 1u), static_cast<uint32_t>(t));
+    mbar_arrive(tile_full0 + 8u * s);
+    mbar_arrive_cluster(mapa_shared(tile_full0 + 8u * s, 1u));
+    return t;
+  };
+  // (every other reader thread) entry e >= 1, or -2 when the wait ran out
+  auto clc_read = [&](int e) -> int {
+    const uint32_t s = static_cast<uint32_t>(e - 1) & 1u;
+    const uint32_t ph = (static_cast<uint32_t>(e - 1) >> 1) & 1u;
+    if (!bounded_wait_cluster(tile_full0 + 8u * s, ph, abort_flag, p.err, kDevTimeoutClc))
+      return -2;
+    const int t = ld_shared_s32(tile_ring0 + 4u * s);
+    if (leader)
+      mbar_arrive(tile_empty0 + 8u * s);
+    else
+      mbar_arrive_cluster(mapa_shared(tile_empty0 + 8u * s, 0u));
+    return t;
+  };
+  // The i-th unit of this thread's walk; false at its end, or when a wait ran
+  // out (the abort flag is then up).
+  auto walk = [&](int i, Unit &u, bool publisher) -> bool {
+    if (!clc) return unit_of(p, unit, units, i, u);
+    if (i == 0) {
+      u = Unit{unit, 0, p.k_blocks, -1};
+      return true;
+    }
+    const int t = publisher ? clc_publish(i) : clc_read(i);
+    if (t == -2) abort_peer();
+    if (t < 0) return false;
+    u = Unit{t, 0, p.k_blocks, -1};
+    return true;
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // multicast: every empty barrier takes both pairs' MMA commits
@@ -568,6 +655,13 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       mbar_init(acc_empty0 + 8u * b, (PAIR ? 2 : 1) * kEpiWarps);
     }
     mbar_init(mma_drained, 1);
+    if (clc) {
+      mbar_init(clc_full, 1);
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(tile_full0 + 8u * s, 1);
+        mbar_init(tile_empty0 + 8u * s, kClcReaders);
+      }
+    }
     if (ASPLIT) {
       for (int s = 0; s < STAGES; ++s) {
         mbar_init(a_full0 + 8u * s, 1);
@@ -608,7 +702,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
     // ------------------------------- panel splitters (in-kernel panel split)
     // Split the caller's A and B into the workspace, item by item, ahead of
     // every CTA's producer (see TcArgs::split_inline).
-    run_splitter<PASSES>(p, units, lane, abort_flag);
+    run_splitter<PASSES>(p, walk_units, lane, abort_flag);
   } else if (ASPLIT && warp >= 2 + kEpiWarps) {
     // --------------------------------------- A-split warps (in-kernel split)
     // Each of the two warps converts half of every landed raw A tile in place:
@@ -733,7 +827,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       bool ok = true;
       bool all_split = false;  // in-kernel split: every item of the launch is done
       Unit u;
-      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+      if (clc && leader) clc_request();  // the answer is needed after this tile's loads
+      for (int i = 0; ok && walk(i, u, leader); ++i) {
         int tm, tn;
         tile_coords(u.tile, tm, tn);
         const int m0 = tm * kTileM + static_cast<int>(rank) * kBM;
@@ -797,6 +892,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
           last_parity = (last_parity & ~(1u << s)) | (ph << s);
         }
       }
+      // A cancel request still in flight (only after an abort) writes its
+      // answer into shared memory: let it land before the CTA exits.
+      if (clc_pending) bounded_wait(clc_full, clc_phase, abort_flag, p.err, kDevTimeoutDrain, false);
       // No bulk copy may still be writing shared memory at exit.  The leader's
       // full barriers count every armed stage; a pair's peer cannot observe its
       // own copies, so after an abort it gives them a bounded grace period.
@@ -821,7 +919,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       int c_glob = 0;  // partial sums produced: TMEM buffer and its phase
       bool ok = true;
       Unit u;
-      for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+      for (int i = 0; ok && walk(i, u, false); ++i) {
         int kb = u.k_lo;
         const int n_chunks = (u.k_hi - u.k_lo + chunk - 1) / chunk;
         for (int c = 0; c < n_chunks && ok; ++c, ++c_glob) {
@@ -944,7 +1042,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
     Unit u;
     constexpr int kRanks = PAIR ? 2 : 1;
     float *sbuf = epi_stage + (warp - 2) * 32 * 32;  // this warp's 32 x 32 block of C
-    for (int i = 0; ok && unit_of(p, unit, units, i, u); ++i) {
+    for (int i = 0; ok && walk(i, u, false); ++i) {
       int tm, tn;
       tile_coords(u.tile, tm, tn);
       // This warp owns rows row0 .. row0+31 and columns col0 .. col0+kHalf-1 of

@@ -121,8 +121,9 @@ def test_plan_raster_groups(lib):
 
 
 def test_kernel_clock_reader_rejects_null(lib):
-    # argument check before any device call
+    # argument checks before any device call
     assert lib.phobos_kernel_clock_mhz(None) == phobos.PHOBOS_ERR_INVALID_VALUE
+    assert lib.phobos_kernel_clc_tiles(None) == phobos.PHOBOS_ERR_INVALID_VALUE
 
 
 def test_plan_rejects_unknown_math(lib):
@@ -167,6 +168,33 @@ def test_multicast_plans_are_validated_before_any_device_call(lib):
     single.multicast, single.cluster_n = 1, 2                      # single CTAs: no pairs
     assert phobos.phobos_sgemm_ex(128, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0,
                                   phobos.PHOBOS_MATH_3XTF32, single) == phobos.PHOBOS_ERR_UNSUPPORTED
+
+
+def test_cluster_launch_control_plans_are_validated_before_any_device_call(lib):
+    # clc = 1: split-TF32 CTA pairs reading A from the workspace only
+    M = N = K = 1024
+
+    def run(plan, math=phobos.PHOBOS_MATH_3XTF32, m=M):
+        return phobos.phobos_sgemm_ex(m, N, K, 1.0, 16, K, 16, N, 0.0, 16, N, 0, math, plan)
+
+    def clc(math="3xtf32", m=M, **fields):
+        p = phobos.phobos_gemm_plan(m, N, K, K, N, N, math)
+        p.clc = 1
+        for name, value in fields.items():
+            setattr(p, name, value)
+        return p
+
+    assert phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32").clc == 0  # never chosen by itself
+    assert run(clc(clc=2)) == phobos.PHOBOS_ERR_INVALID_VALUE
+    assert run(clc(a_split=2)) == phobos.PHOBOS_ERR_UNSUPPORTED    # A split in shared memory
+    assert run(clc(multicast=1, cluster_n=2)) == phobos.PHOBOS_ERR_UNSUPPORTED
+    assert run(clc("tf32"), phobos.PHOBOS_MATH_TF32) == phobos.PHOBOS_ERR_UNSUPPORTED
+    assert run(clc("bf16"), phobos.PHOBOS_MATH_BF16) == phobos.PHOBOS_ERR_UNSUPPORTED
+    single = clc(m=128)
+    assert single.cluster_m == 1
+    assert run(single, m=128) == phobos.PHOBOS_ERR_UNSUPPORTED     # CTA pairs only
+    ffma = clc("ffma")
+    assert run(ffma, phobos.PHOBOS_MATH_FFMA) == phobos.PHOBOS_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("var", ["WORLD_SIZE", "LOCAL_WORLD_SIZE"])

@@ -33,21 +33,28 @@ def dev():
     return d
 
 
-@pytest.mark.parametrize("shape,multicast,a_split,withhold", [
-    ((128, 256, 96), 0, 0, "LOAD"), ((256, 256, 96), 0, 0, "LOAD"), ((256, 512, 96), 1, 0, "LOAD"),
-    ((256, 256, 96), 0, 3, "LOAD"), ((256, 256, 96), 0, 3, "SPLIT")],
-    ids=["single_cta", "cta_pair", "multicast_cluster", "panel_split", "panel_split_flag"])
+@pytest.mark.parametrize("shape,multicast,a_split,withhold,clc", [
+    ((128, 256, 96), 0, 0, "LOAD", 0), ((256, 256, 96), 0, 0, "LOAD", 0),
+    ((256, 512, 96), 1, 0, "LOAD", 0), ((256, 256, 96), 0, 3, "LOAD", 0),
+    ((256, 256, 96), 0, 3, "SPLIT", 0), ((2560, 2048, 96), 0, 1, "LOAD", 1),
+    ((2560, 2048, 96), 0, 3, "LOAD", 1)],
+    ids=["single_cta", "cta_pair", "multicast_cluster", "panel_split", "panel_split_flag",
+         "cluster_launch_control", "cluster_launch_control_panel_split"])
 def test_expired_wait_is_reported_and_context_survives(dev, shape, multicast, a_split, withhold,
-                                                       monkeypatch):
+                                                       clc, monkeypatch):
     # withhold = LOAD: the producer skips its first operand load and the MMA
     # issuer's wait expires; SPLIT (in-kernel panel split): the splitter never
     # publishes its first item's flag and the producer's wait for it expires.
+    # With Cluster Launch Control (clc = 1) the 80 tiles outnumber the pairs
+    # that fit at once: every pair times out on its first tile, after its
+    # leader has asked for (and may have cancelled) a pair not yet launched.
     M, N, K = shape
     plan = phobos.phobos_gemm_plan(M, N, K, K, N, N, "3xtf32")
     assert plan.cluster_m == (2 if M > 128 else 1)
     if multicast:  # two CTA pairs sharing A through TMA multicast
         plan.multicast, plan.cluster_n = 1, 2
     plan.a_split = a_split  # 3: A and B split by the GEMM kernel's splitter warps
+    plan.clc = clc
     A = si.normal(71, 0, (M, K))
     B = si.normal(71, 1, (K, N))
     dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
