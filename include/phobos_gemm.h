@@ -171,13 +171,19 @@ typedef enum {
  *                  own tile and then takes tiles from the hardware's queue of
  *                  pairs not yet launched (it cancels their launch), so pairs
  *                  that finish early, or start late because other work holds
- *                  SMs, take more tiles.  The tail split is off (tail_split
- *                  is ignored); with a_split = 0 the kernel splits A and B
- *                  itself.  Each tile's result equals the static walk's with
- *                  tail_split = 1, bit for bit.  0 (the planner's choice) =
- *                  a static persistent walk: one pair per SM pair, tiles
- *                  strided over the pairs.  Other plans with clc = 1 give
- *                  PHOBOS_ERR_UNSUPPORTED.
+ *                  SMs, take more tiles.  With a_split = 0 the kernel splits
+ *                  A and B itself.  tail_split cuts the tiles of the last
+ *                  partial wave into K pieces (0: enough to give every
+ *                  resident pair work, at most 8, each at least 4 k blocks;
+ *                  1: off; 2..8: that many), each dealt like a tile: every
+ *                  piece leaves its partial sum in the workspace and the
+ *                  last to finish adds them in K order and stores the tile,
+ *                  so no piece waits for another and the result is
+ *                  deterministic.  With tail_split = 1 each tile's result
+ *                  equals the static walk's (tail_split = 1) bit for bit.
+ *                  0 (the planner's choice) = a static persistent walk: one
+ *                  pair per SM pair, tiles strided over the pairs.  Other
+ *                  plans with clc = 1 give PHOBOS_ERR_UNSUPPORTED.
  *  FP16 and BF16 plans run the tensor-core kernel with its deepest stage ring
  *  only (stages must equal the planner's value).
  */

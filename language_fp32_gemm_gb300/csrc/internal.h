@@ -141,10 +141,15 @@ struct TcArgs {
   // split or multicast).  1: the grid holds one pair per output tile; a
   // resident pair starts on its own tile and takes every further tile from
   // the hardware by cancelling the launch of a pair that has not started, so
-  // tiles are dealt to pairs as they free up.  No tail split.  clc_units:
-  // the pairs that fit on the device at once (the in-kernel split orders its
-  // items by their waves).
-  int clc, clc_units;
+  // tiles are dealt to pairs as they free up.  clc_units: the pairs that fit
+  // on the device at once (the in-kernel split orders its items by their
+  // waves).  clc_pieces P > 1: work items [0, full_tiles) are whole tiles,
+  // and item full_tiles + j * P + q is K piece q (k blocks [q kb / P,
+  // (q+1) kb / P)) of tile full_tiles + j.  Every piece leaves its partial sum
+  // in partials slot j * P + q and counts itself in on the tile's counter
+  // flags[(j * 2 + rank) * 8 + warp - 2]; the last to arrive adds the P slots
+  // in order, stores C and resets the counter.  No piece waits for another.
+  int clc, clc_units, clc_pieces;
   // Instrumentation (nullptr = off): thread 0 of CTA 0 adds the SM cycles
   // (clock64) and the nanoseconds (%globaltimer) of its CTA's lifetime to
   // clock_acc[0] and clock_acc[1], which gives the SM clock the kernel ran at;

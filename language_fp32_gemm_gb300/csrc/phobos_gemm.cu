@@ -395,10 +395,8 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
   if (p.a_split < 0 || p.a_split > 3) return PHOBOS_ERR_INVALID_VALUE;
   if (p.clc != 0 && p.clc != 1) return PHOBOS_ERR_INVALID_VALUE;
   // Cluster Launch Control deals tiles to split-TF32 CTA pairs that read A
-  // from the workspace (the kernel's barrier block has room for its state at
-  // that ring depth)
-  if (p.clc == 1 &&
-      (p.cluster_m != 2 || mc || p.path != PHOBOS_PATH_3XTF32 || p.a_split == 2 || p.stages > 4))
+  // from the workspace, with the deepest ring (checked below)
+  if (p.clc == 1 && (p.cluster_m != 2 || mc || p.path != PHOBOS_PATH_3XTF32 || p.a_split == 2))
     return PHOBOS_ERR_UNSUPPORTED;
   // the in-kernel panel split runs in tf32 CTA pairs without multicast
   if (p.a_split == 3 && (p.cluster_m != 2 || mc ||
@@ -418,7 +416,7 @@ phobos_status_t validate_plan(int64_t M, int64_t N, int64_t K, phobos_math_t mat
       return PHOBOS_ERR_INVALID_VALUE;
     const int max_st = pair ? tc_pair_max_stages(passes, p.tile_n) : tc_max_stages(passes, p.tile_n);
     if (p.stages < 2 || p.stages > max_st) return PHOBOS_ERR_INVALID_VALUE;
-    if ((p.a_split >= 2 || mc) && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
+    if ((p.a_split >= 2 || mc || p.clc) && p.stages != max_st) return PHOBOS_ERR_INVALID_VALUE;
     // 16-bit inputs: pre-converted A, deepest ring
     if (half_path(p.path) && (p.a_split == 2 || (p.stages != max_st && p.stages != 4)))
       return PHOBOS_ERR_INVALID_VALUE;
@@ -556,7 +554,19 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int tail = units > 0 && !p.clc ? total_tiles % units : 0;
   const int tail_units = tail_workers(p.tail_split, tail, units, chunk_blocks_max);
   const int full_tiles = tail_units > 0 ? total_tiles - tail : total_tiles;
-  const int64_t slots = static_cast<int64_t>(tail_units) * (mc ? 2 : 1);  // one partial sum per pair at most
+  // Cluster Launch Control: the last partial wave's tiles cut into P K
+  // pieces of at least 4 k blocks, enough to give every resident pair work
+  // (tail_split 1: off; 2..8: P)
+  int clc_pieces = 1;
+  const int clc_tail = p.clc && units > 0 ? total_tiles % units : 0;
+  if (clc_tail > 0 && p.tail_split != 1) {
+    int P = p.tail_split >= 2 ? p.tail_split : units / clc_tail;
+    if (P > chunk_blocks_max / 4) P = chunk_blocks_max / 4;
+    if (P > kMaxTailSplit) P = kMaxTailSplit;
+    clc_pieces = P > 1 ? P : 1;
+  }
+  const int64_t slots = clc_pieces > 1 ? static_cast<int64_t>(clc_tail) * clc_pieces
+                                       : static_cast<int64_t>(tail_units) * (mc ? 2 : 1);
   const size_t part_bytes = static_cast<size_t>(round_up(slots * bm * bn * 4, 256));
   // flags: the tail split's, then (in-kernel panel split) one per item of the
   // longest launch and two item counters per launch (claimed, done)
@@ -691,10 +701,12 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   // workers sharing the tail are launched
   t.grid_units = tail_units > 0 ? (full_tiles > 0 ? units : tail_units)
                                 : (total_tiles < units ? total_tiles : units);
-  if (p.clc) {  // a pair per tile; the resident ones take the rest
+  if (p.clc) {  // a pair per work item; the resident ones take the rest
     t.clc = 1;
     t.clc_units = units;
-    t.grid_units = total_tiles;
+    t.clc_pieces = clc_pieces;
+    t.full_tiles = clc_pieces > 1 ? total_tiles - clc_tail : total_tiles;
+    t.grid_units = t.full_tiles + (clc_pieces > 1 ? clc_tail * clc_pieces : 0);
   }
   t.partials = partials;
   t.flags = flags;

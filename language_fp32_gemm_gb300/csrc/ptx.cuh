@@ -486,6 +486,14 @@ __device__ __forceinline__ void st_release_gpu(unsigned *addr, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
+// Atomic add at GPU scope with acquire and release semantics; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Add v at GPU scope with release semantics: this thread's earlier writes
 // (and those its fences cover) are visible to whoever acquires the sum.
 __device__ __forceinline__ void red_release_gpu_add(unsigned *addr, unsigned v) {

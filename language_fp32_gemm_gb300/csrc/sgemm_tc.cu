@@ -476,7 +476,7 @@ __device__ __forceinline__ bool wait_split_chunk(const TcArgs &p, int tm, int tn
 }
 
 template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32,
-          bool MC = false, bool INL = false>
+          bool MC = false, bool INL = false, bool CLC = false>
 __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
     sgemm_tc_kernel(const __grid_constant__ TcArgs p) {
   using S = TcShape<BN, PASSES, PAIR>;
@@ -500,7 +500,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   // Cluster Launch Control state after the abort flag (16-byte aligned): the
   // hardware's answer and its barrier, then a two-entry ring of tile indices
   // with full barriers (both CTAs) and empty barriers (the leader's).
-  constexpr bool kClcKernel = PAIR && !ASPLIT && !MC && (4 * STAGES + 5) * 8 + 8 + 64 <= 256;
+  static_assert(!CLC || (PAIR && !ASPLIT && !MC && (4 * STAGES + 5) * 8 + 8 + 64 <= 256),
+                "Cluster Launch Control: CTA pairs without multicast or the A split in shared "
+                "memory, and room for its state in the barrier block");
   const uint32_t clc_resp = smem_u32(tmem_slot + 2);
   const uint32_t clc_full = clc_resp + 16u;
   const uint32_t tile_full0 = clc_resp + 24u;
@@ -575,7 +577,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
   // peer's producer and every thread of the accumulator warps read the ring
   // and release the entry on the leader, one arrival each.  Entry -1 ends the
   // walk.
-  const bool clc = kClcKernel && p.clc != 0;
+  constexpr bool clc = CLC;
   constexpr int kClcReaders = 2 * (1 + 32 * kEpiWarps);
   // the units the in-kernel split's item order expects to run at once
   const int walk_units = clc ? p.clc_units : units;
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       const int x = clc_cancelled_ctaid_x(clc_resp);
       if (x >= 0) {
         t = x / 2;  // the first CTA of a pair has an even index
-        if (t >= p.tiles_m * p.tiles_n) {  // not a tile of this grid: stop, and say so
+        if (t >= p.grid_units) {  // not a work item of this grid: stop, and say so
           *abort_flag = 1;
           atomicCAS(p.err, 0, kDevTimeoutClc);
           return -2;
@@ -629,18 +631,29 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       mbar_arrive_cluster(mapa_shared(tile_empty0 + 8u * s, 0u));
     return t;
   };
+  // Work item t of the grid: a whole tile, or (with clc_pieces > 1) a K
+  // piece of a tile of the last partial wave (piece code 2 + q).
+  auto clc_unit = [&](int t, Unit &u) {
+    const int P = p.clc_pieces;
+    if (P > 1 && t >= p.full_tiles) {
+      const int r = t - p.full_tiles, j = r / P, qq = r - j * P;
+      u = Unit{p.full_tiles + j, qq * p.k_blocks / P, (qq + 1) * p.k_blocks / P, 2 + qq};
+    } else {
+      u = Unit{t, 0, p.k_blocks, -1};
+    }
+  };
   // The i-th unit of this thread's walk; false at its end, or when a wait ran
   // out (the abort flag is then up).
   auto walk = [&](int i, Unit &u, bool publisher) -> bool {
-    if (!clc) return unit_of(p, unit, units, i, u);
+    if constexpr (!CLC) return unit_of(p, unit, units, i, u);
     if (i == 0) {
-      u = Unit{unit, 0, p.k_blocks, -1};
+      clc_unit(unit, u);
       return true;
     }
     const int t = publisher ? clc_publish(i) : clc_read(i);
     if (t == -2) abort_peer();
     if (t < 0) return false;
-    u = Unit{t, 0, p.k_blocks, -1};
+    clc_unit(t, u);
     return true;
   };
 
@@ -894,7 +907,8 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       }
       // A cancel request still in flight (only after an abort) writes its
       // answer into shared memory: let it land before the CTA exits.
-      if (clc_pending) bounded_wait(clc_full, clc_phase, abort_flag, p.err, kDevTimeoutDrain, false);
+      if (CLC && clc_pending)
+        bounded_wait(clc_full, clc_phase, abort_flag, p.err, kDevTimeoutDrain, false);
       // No bulk copy may still be writing shared memory at exit.  The leader's
       // full barriers count every armed stage; a pair's peer cannot observe its
       // own copies, so after an abort it gives them a bounded grace period.
@@ -1050,9 +1064,9 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       const int tile_row = static_cast<int>(rank) * kBM + q * 32 + lane;  // 0 .. kTileM-1
       const int row0 = tm * kTileM + tile_row - lane;
       const int col0 = tn * BN + h * kHalf;
-      const bool writes_c = u.piece <= 0 && row0 < p.M && col0 < p.N;  // warp-uniform
-      const bool vec = p.vec_c && col0 + kHalf <= p.N;                  // 16-byte rows
-      const bool load_old = writes_c && p.beta != 0.0f;
+      bool writes_c = u.piece <= 0 && row0 < p.M && col0 < p.N;  // warp-uniform
+      const bool vec = p.vec_c && col0 + kHalf <= p.N;            // 16-byte rows
+      bool load_old = writes_c && p.beta != 0.0f;
       // Old C of columns j0 .. j0+31 into the warp's block, in the swizzled
       // layout the row-per-lane reads below use: row r, column c at
       // r*32 + (c ^ r) (4-byte copies), or 16-byte chunk ch at chunk ch ^ (r & 7).
@@ -1121,7 +1135,59 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
       // Tail pieces exchange their partial sums through L2 in a warp-interleaved
       // layout: float4 v of lane l of a warp sits at (v * 32 + l), so that every
       // store and load instruction covers 512 contiguous bytes.
-      if (u.piece > 0) {
+      if (CLC && u.piece >= 2) {
+        // Cluster Launch Control tail piece q = piece - 2 of tail tile jt (see
+        // TcArgs::clc_pieces): leave the partial sum in slot jt * P + q and count
+        // in on the tile's counter; the last piece to arrive adds the P slots in
+        // K order and stores C.  No piece waits for another, so no piece can
+        // hold up a tile that the hardware has not dealt yet.
+        const int P = p.clc_pieces, jt = u.tile - p.full_tiles;
+        constexpr int kSlotF4 = kHalf / 4;  // float4 per lane per piece
+        constexpr long long kSlotStride = static_cast<long long>(kRanks) * kEpiWarps * kSlotF4 * 32;
+        float4 *const first = reinterpret_cast<float4 *>(p.partials) +
+                              ((static_cast<long long>(jt) * P * kRanks + rank) * kEpiWarps +
+                               (warp - 2)) * (kSlotF4 * 32) + lane;
+        float4 *const mine = first + (u.piece - 2) * kSlotStride;
+#pragma unroll
+        for (int v = 0; v < kSlotF4; ++v)
+          __stcg(mine + v * 32, make_float4(sum[4 * v], sum[4 * v + 1], sum[4 * v + 2], sum[4 * v + 3]));
+        __threadfence();
+        __syncwarp();
+        unsigned *const counter = p.flags + (static_cast<long long>(jt) * 2 + rank) * kEpiWarps + (warp - 2);
+        unsigned old = 0;
+        if (lane == 0) old = atom_add_acq_rel_gpu(counter, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old + 1u != static_cast<unsigned>(P)) continue;  // a later piece finishes the tile
+        (void)ld_acquire_gpu(counter);  // every lane acquires the other pieces' stores
+#pragma unroll
+        for (int v0 = 0; v0 < kSlotF4; v0 += 8) {
+#pragma unroll 1
+          for (int qq = 0; qq < P; ++qq) {
+            float4 x[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) x[t] = __ldcg(first + qq * kSlotStride + (v0 + t) * 32);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int e = 4 * (v0 + t);
+              if (qq == 0) {
+                sum[e] = x[t].x;
+                sum[e + 1] = x[t].y;
+                sum[e + 2] = x[t].z;
+                sum[e + 3] = x[t].w;
+              } else {
+                sum[e] = __fadd_rn(sum[e], x[t].x);
+                sum[e + 1] = __fadd_rn(sum[e + 1], x[t].y);
+                sum[e + 2] = __fadd_rn(sum[e + 2], x[t].z);
+                sum[e + 3] = __fadd_rn(sum[e + 3], x[t].w);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) *counter = 0u;  // ready for the next launch's pieces of this tile
+        writes_c = row0 < p.M && col0 < p.N;
+        load_old = writes_c && p.beta != 0.0f;
+      } else if (u.piece > 0) {
         // Hand the partial sum to the piece-0 owner through this worker's
         // slot, then release the flag once every accumulator thread's stores
         // are visible.
@@ -1311,7 +1377,7 @@ __global__ void __launch_bounds__(threads_for(ASPLIT || INL), 1)
 // Launch configuration of one kernel instance: the persistent grid of `units`
 // CTAs, CTA pairs, or (multicast) clusters of two pairs.
 template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND, bool MC,
-          bool INL = false>
+          bool INL = false, bool CLC = false>
 void tc_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, unsigned units,
                cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
@@ -1330,11 +1396,11 @@ void tc_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attr, unsigned unit
 }
 
 template <int BN, int PASSES, int STAGES, bool PAIR, bool ASPLIT, int KIND = kTcTf32,
-          bool MC = false, bool INL = false>
+          bool MC = false, bool INL = false, bool CLC = false>
 cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   using S = TcShape<BN, PASSES, PAIR>;
   static_assert(STAGES >= 2 && STAGES <= S::max_stages(), "stage ring does not fit");
-  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC, INL>;
+  auto kern = sgemm_tc_kernel<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC, INL, CLC>;
   const int smem = S::smem_bytes(STAGES);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1351,7 +1417,7 @@ cudaError_t launch_one(const TcArgs &a, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  tc_config<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC, INL>(cfg, attr, units, stream);
+  tc_config<BN, PASSES, STAGES, PAIR, ASPLIT, KIND, MC, INL, CLC>(cfg, attr, units, stream);
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
@@ -1396,6 +1462,17 @@ cudaError_t launch_stages(const TcArgs &a, int stages, cudaStream_t stream, int 
     if constexpr (PAIR) {
       if (a.a_inline || a.split_inline || stages != kTop) return cudaErrorInvalidValue;
       return launch_one<BN, PASSES, kTop, true, false, kTcTf32, true>(a, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
+  // Cluster Launch Control (split-TF32 CTA pairs reading A from the
+  // workspace): the deepest ring, with or without the in-kernel panel split.
+  if (a.clc) {
+    if constexpr (PAIR && PASSES == 3) {
+      if (a.a_inline || stages != kTop) return cudaErrorInvalidValue;
+      return a.split_inline
+                 ? launch_one<BN, 3, kTop, true, false, kTcTf32, false, true, true>(a, stream)
+                 : launch_one<BN, 3, kTop, true, false, kTcTf32, false, false, true>(a, stream);
     }
     return cudaErrorInvalidValue;
   }

@@ -4,9 +4,12 @@ The grid holds one CTA pair per output tile; the pairs that fit on the GPU
 start on their own tiles and take the others from the hardware by
 cancelling the launch of pairs that have not started ("Clusters et DSMEM",
 3.7, Cluster Launch Control).  Each tile is computed whole, in the same order
-of operations as the static persistent walk without the tail split, so the
-result must equal that walk's (tail_split = 1) bit for bit, whichever way A
-and B are split, and the oracle's within the split-TF32 bound.  Shapes run
+of operations as the static persistent walk without the tail split, so with
+tail_split = 1 the result must equal that walk's bit for bit, whichever way
+A and B are split, and the oracle's within the split-TF32 bound.  By default
+the last partial wave's tiles are cut into K pieces, added by whichever piece
+finishes last in a fixed order: checked against the oracle and against a
+repeat run, bit for bit.  Shapes run
 from one tile (every request cancels nothing) to far more tiles than pairs
 fit at once (most tiles come from cancelled launches), with ragged edges,
 padded leading dimensions and K-chunked launches.
@@ -60,7 +63,7 @@ def test_clc_equals_the_static_walk_bitwise(dev, shape, a_split):
     B = si.normal(121, 1, (K, N))
     C0 = si.uniform_pm1(121, 2, (M, N))
     C = run_gemm(torch, dev, A, B, C0, 1.25, 0.5, "3xtf32",
-                 plan=plan_for(M, N, K, K, N, N, clc=1, a_split=a_split))
+                 plan=plan_for(M, N, K, K, N, N, clc=1, tail_split=1, a_split=a_split))
     S = run_gemm(torch, dev, A, B, C0, 1.25, 0.5, "3xtf32",
                  plan=plan_for(M, N, K, K, N, N, tail_split=1, a_split=a_split))
     ref, den = oracle.sgemm(A, B, C0, 1.25, 0.5)
@@ -89,12 +92,47 @@ def test_clc_in_the_k_chunked_mode(dev, super_k):
     B = si.normal(123, 1, (K, N))
     C0 = si.uniform_pm1(123, 2, (M, N))
     C = run_gemm(torch, dev, A, B, C0, 1.0, 0.5, "3xtf32",
-                 plan=plan_for(M, N, K, K, N, N, clc=1, super_k=super_k))
+                 plan=plan_for(M, N, K, K, N, N, clc=1, tail_split=1, super_k=super_k))
     S = run_gemm(torch, dev, A, B, C0, 1.0, 0.5, "3xtf32",
                  plan=plan_for(M, N, K, K, N, N, tail_split=1, super_k=super_k))
+    P = run_gemm(torch, dev, A, B, C0, 1.0, 0.5, "3xtf32",
+                 plan=plan_for(M, N, K, K, N, N, clc=1, super_k=super_k))  # tail pieces
     ref, den = oracle.sgemm(A, B, C0, 1.0, 0.5)
     assert oracle.max_rel_error(C, ref, den) <= oracle.TOL_FP32
+    assert oracle.max_rel_error(P, ref, den) <= oracle.TOL_FP32
     assert np.array_equal(bits(C), bits(S))
+
+
+# tail tiles: 4 of 80 (cut into 8 pieces), 28 of 256 (2 pieces), 12 of 240 (6)
+TAIL_SHAPES = [(2560, 2048, 2048), (4096, 4096, 1024), (3001, 5003, 1999)]
+
+
+@pytest.mark.parametrize("tail_split", [0, 3, 8], ids=["auto", "3_pieces", "8_pieces"])
+@pytest.mark.parametrize("shape", TAIL_SHAPES, ids=["x".join(map(str, s)) for s in TAIL_SHAPES])
+def test_clc_tail_pieces_match_the_oracle_and_repeat_bitwise(dev, shape, tail_split):
+    # The last partial wave's tiles are cut into K pieces; every piece leaves
+    # its partial sum behind and the last one to finish adds them in K order,
+    # so the result does not depend on which piece finishes last.
+    M, N, K = shape
+    A = si.normal(126, 0, (M, K))
+    B = si.normal(126, 1, (K, N))
+    C0 = si.uniform_pm1(126, 2, (M, N))
+    plan = plan_for(M, N, K, K, N, N, clc=1, tail_split=tail_split)
+    C1 = run_gemm(torch, dev, A, B, C0, 1.25, 0.5, "3xtf32", plan=plan)
+    C2 = run_gemm(torch, dev, A, B, C0, 1.25, 0.5, "3xtf32", plan=plan)
+    ref, den = oracle.sgemm(A, B, C0, 1.25, 0.5)
+    assert oracle.max_rel_error(C1, ref, den) <= oracle.TOL_FP32
+    assert np.array_equal(bits(C1), bits(C2))
+
+
+def test_clc_tail_pieces_integer_inputs_are_exact(dev):
+    M, N, K = 4096, 4096, 1024  # 28 tail tiles in 2 pieces each
+    A = si.integers(127, 0, (M, K))
+    B = si.integers(127, 1, (K, N))
+    C0 = si.integers(127, 2, (M, N))
+    C = run_gemm(torch, dev, A, B, C0, 1.5, 0.5, "3xtf32", plan=plan_for(M, N, K, K, N, N, clc=1))
+    ref, _ = oracle.sgemm(A, B, C0, 1.5, 0.5, want_den=False)
+    assert np.array_equal(C, ref.astype(np.float32))  # integer sums below 2^24: exact
 
 
 def test_clc_integer_inputs_are_exact_over_many_tiles(dev):
@@ -120,7 +158,7 @@ def test_clc_tiles_come_from_cancelled_launches(dev, shape):
     dA = torch.from_numpy(si.normal(125, 0, (M, K))).to(dev)
     dB = torch.from_numpy(si.normal(125, 1, (K, N))).to(dev)
     dC = torch.zeros((M, N), dtype=torch.float32, device=dev)
-    plan = plan_for(M, N, K, K, N, N, clc=1)
+    plan = plan_for(M, N, K, K, N, N, clc=1, tail_split=1)  # whole tiles only
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()  # torch creates the CUDA events on their first record
     stop.record()
