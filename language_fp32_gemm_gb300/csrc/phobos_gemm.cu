@@ -550,7 +550,7 @@ phobos_status_t run_tc(int64_t M, int64_t N, int64_t K, float alpha, const float
   const int total_tiles = static_cast<int>((Mp / bm) * walk_n);
   const int chunk_blocks_max =
       static_cast<int>(round_up(p.super_k < K ? p.super_k : K, bk) / bk);
-  // (Cluster Launch Control: whole tiles only, dealt by the hardware)
+  // the static walk's tail split (Cluster Launch Control cuts its own, below)
   const int tail = units > 0 && !p.clc ? total_tiles % units : 0;
   const int tail_units = tail_workers(p.tail_split, tail, units, chunk_blocks_max);
   const int full_tiles = tail_units > 0 ? total_tiles - tail : total_tiles;
