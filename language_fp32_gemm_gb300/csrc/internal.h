@@ -159,7 +159,9 @@ struct TcArgs {
 };
 // K blocks per item of the in-kernel panel split (256 of K).  Measured on
 // GB300: items of 64 of K spent more time in their flag fences and round trips
-// than they saved at the start (4096^3: 0.542 against 0.447 ms per call).
+// than they saved at the start (4096^3: 0.542 against 0.447 ms per call), and
+// items of 128 of K still did (4096^3 0.455 against 0.433 ms, 8192^3 3.11
+// against 3.04 ms).
 constexpr int kSplitChunkBlocks = 8;
 // Operand types of the tensor-core kernel: tf32 from fp32 containers (one or
 // three passes), or pre-converted fp16 / bf16 (one pass, MMA kind::f16).
