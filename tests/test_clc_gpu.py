@@ -174,3 +174,29 @@ def test_clc_tiles_come_from_cancelled_launches(dev, shape):
     assert tiles - 76 <= n <= tiles - 1, (n, tiles)
     phobos.sgemm(dA, dB, dC, 1.0, 0.0, math="3xtf32", plan=plan)
     assert phobos.phobos_kernel_clc_tiles() == 0  # not timed: not counted
+
+
+def test_clc_beside_work_on_another_stream(dev):
+    # Matrix products queued on another stream may hold SMs when the GEMM
+    # starts: pairs that do not fit start later, and the hardware deals the
+    # remaining tiles to the pairs that run.  Each tile is computed the same
+    # way whoever takes it, so the result equals the static walk's.
+    M, N, K = 4096, 4096, 1024
+    A = si.normal(128, 0, (M, K))
+    B = si.normal(128, 1, (K, N))
+    C0 = si.uniform_pm1(128, 2, (M, N))
+    dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    dC = torch.from_numpy(C0).to(dev)
+    X = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    other = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(other):
+        for _ in range(4):
+            X @ X
+    phobos.sgemm(dA, dB, dC, 1.0, 0.5, math="3xtf32",
+                 plan=plan_for(M, N, K, K, N, N, clc=1, tail_split=1))
+    torch.cuda.synchronize()
+    assert phobos.phobos_check_device(0) == phobos.PHOBOS_OK
+    S = run_gemm(torch, dev, A, B, C0, 1.0, 0.5, "3xtf32",
+                 plan=plan_for(M, N, K, K, N, N, tail_split=1))
+    assert np.array_equal(bits(dC.cpu().numpy()), bits(S))
