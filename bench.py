@@ -59,7 +59,9 @@ def parse_args():
                     help="device-resident steps deal tiles to CTA pairs through Cluster Launch "
                          "Control (plan clc = 1, split TF32 only) instead of the static "
                          "persistent walk; the e2e leg keeps the automatic plan")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10,
+                    help="timed calls of the host-buffer leg (after one untimed call); their "
+                         "mean is the e2e rate")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target host time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -503,7 +505,8 @@ def run_phobos(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": sum(e2e_ms) / len(e2e_ms),
-                "api": "phobos_sgemm_host (pinned host buffers)"} if e2e_ms else None,
+                "steps": len(e2e_ms), "api": "phobos_sgemm_host (pinned host buffers)"}
+               if e2e_ms else None,
         "gpu_launches": int(launches),
         "clocks": clk,
     }
