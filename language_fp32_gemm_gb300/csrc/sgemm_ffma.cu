@@ -58,7 +58,28 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 1)
   float a_reg[A_LOADS][4];
   float b_reg[B_LOADS][4];
 
+  // Tiles wholly inside the matrix (the common case) load without the
+  // per-element bounds checks.
+  const bool a_rows_in = p.vec_a && m0 + BM <= p.M;
+  const bool b_cols_in = p.vec_b && n0 + BN <= p.N;
   auto load_tiles = [&](int k0) {
+    if (k0 + kBK <= k_hi && a_rows_in && b_cols_in) {
+#pragma unroll
+      for (int l = 0; l < A_LOADS; ++l) {
+        const int g = tid + l * NT;
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(
+            p.A + static_cast<int64_t>(m0 + g / (kBK / 4)) * p.lda + k0 + (g % (kBK / 4)) * 4));
+        a_reg[l][0] = v.x; a_reg[l][1] = v.y; a_reg[l][2] = v.z; a_reg[l][3] = v.w;
+      }
+#pragma unroll
+      for (int l = 0; l < B_LOADS; ++l) {
+        const int g = tid + l * NT;
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(
+            p.B + static_cast<int64_t>(k0 + g / (BN / 4)) * p.ldb + n0 + (g % (BN / 4)) * 4));
+        b_reg[l][0] = v.x; b_reg[l][1] = v.y; b_reg[l][2] = v.z; b_reg[l][3] = v.w;
+      }
+      return;
+    }
 #pragma unroll
     for (int l = 0; l < A_LOADS; ++l) {
       const int g = tid + l * NT;       // group index in the BM x 8 tile
@@ -144,10 +165,11 @@ __global__ void __launch_bounds__((BM / 8) * (BN / 8), BM == 128 ? 2 : 1)
       const float4 b0 = fb[k & 1][0], b1 = fb[k & 1][1];
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      // column-outer order measured 1-2 % faster than row-outer
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     if (more) {
       store_tiles(buf ^ 1);

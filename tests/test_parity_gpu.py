@@ -314,6 +314,28 @@ def test_ffma_cluster_split_k(dev, shape, split):
     assert np.array_equal(C1, C2)  # deterministic
 
 
+# 128 x 128 FFMA tiles: interior K tiles load without bounds checks; the
+# last partial K tile, ragged edge tiles, unaligned bases and leading
+# dimensions that are not multiples of 4 take the checked loads.
+@pytest.mark.parametrize("shape,pads,offsets,super_k", [
+    ((384, 384, 200), (0, 0, 0), (0, 0, 0), None),   # all tiles interior, K tail of 8
+    ((300, 260, 203), (0, 0, 0), (0, 0, 0), None),   # ragged M, N and K
+    ((384, 256, 256), (1, 0, 0), (0, 0, 0), None),   # lda = K + 1: A on the checked loads
+    ((384, 256, 256), (0, 0, 0), (0, 1, 0), None),   # B base not 16-byte aligned
+    ((256, 384, 1000), (0, 0, 0), (0, 0, 0), 520),   # K chunks starting at 8 mod 16
+], ids=lambda v: str(v))
+def test_ffma_128_interior_and_edges(dev, shape, pads, offsets, super_k):
+    M, N, K = shape
+    plan = phobos.phobos_gemm_plan(M, N, K, K + pads[0], N + pads[1], N + pads[2], "ffma")
+    plan.tile_m, plan.tile_n = 128, 128
+    if super_k is not None:
+        plan.super_k = super_k
+    A = padded(si.normal(96, 0, (M, K)), pads[0])
+    B = padded(si.normal(96, 1, (K, N)), pads[1])
+    C0 = padded(si.uniform_pm1(96, 2, (M, N)), pads[2])
+    check(dev, A, B, C0, 1.25, 0.5, "ffma", plan=plan, offsets=offsets)
+
+
 @pytest.mark.parametrize("beta", [0.0, 0.5])
 def test_host_buffer_entry_point_in_bands(dev, beta):
     # M >= 2048 on the tensor-core path: row bands with overlapped copies;
